@@ -1,0 +1,364 @@
+#!/usr/bin/env python
+"""Benchmark: selected-cell (QSA union) prompt attention, query-head rows/s.
+
+One step = the whole hot path over one synthetic prompt chunk resident in HBM:
+union build (qsa_union_build) + union attention (qsa_union_attn).  The workload
+is the 40,960-cell context with an 8,192-position chunk (positions 32,768-40,959),
+4 KV heads x 12 query heads, d = 128, selections capped at 2,051 cells, drift 0.25.
+
+Prints ONE JSON line (rank 0).  `value` = query-head rows/s of the whole job
+(every rank processes its own independent chunk: weak scaling, no collective on
+the data path).  `roofline` describes the attention kernel (the dominant one).
+`e2e` repeats the measurement through the public call with pinned host buffers,
+host->device inputs and device->host outputs inside the timed region.
+`cpu_baseline` times the FP64 CPU oracle on a bounded sample on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "query-head rows/sec at 40K ctx, 2,051-cell cap; achieved % of HBM roofline"
+UNIT = "query-head rows/s"
+CONFIG_ID = 4
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--variant", type=int, default=0, help="0 default, 1 tcgen05, 2 mma.sync")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def workload_desc(w):
+    return (f"{w.name}: {w.ctx:,}-cell context, {w.n_q:,} queries (positions {w.q0:,}-{w.q0 + w.n_q - 1:,}), "
+            f"{w.n_kv} KV heads x 12 query heads, d=128, 64-cell pages behind a shuffled page table, "
+            f"cap 2,051 (3 sinks + 32 blocks), drift {w.drift}")
+
+
+def algorithmic(w, union_count):
+    """Bytes and FLOPs one attention launch must move / do (unpadded, exact unions)."""
+    U = union_count.astype(np.int64)
+    n_rows = w.n_q * w.n_heads
+    kv = int(U.sum()) * w.n_kv * (128 + 128 + 2 + 2)
+    q_out = n_rows * 128 * (2 + 4)
+    union_reads = int(U.sum()) * w.n_kv * 5
+    flops = int(U.sum()) * w.n_kv * 2 * 2 * 96 * 128
+    union_build_bytes = int(w.sel_count.astype(np.int64).sum()) * 4 + int(U.sum()) * 5
+    return dict(bytes=kv + q_out + union_reads, kv_bytes=kv, flops=flops, union_build_bytes=union_build_bytes,
+                mean_union=float(U.mean()), union_ratio=float(U.mean() / w.sel_count.mean()))
+
+
+def read_traffic(kernel: str, sources):
+    """DRAM bytes per launch for `kernel` from the committed ncu summaries, if the
+    kernel's sources still hash to what the capture recorded; else None."""
+    h = hashlib.sha256()
+    for s in sources:
+        h.update(open(os.path.join(ROOT, s), "rb").read())
+    digest = h.hexdigest()[:16]
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None, digest
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".txt"):
+            continue
+        txt = open(os.path.join(pdir, f)).read()
+        m_k = re.search(r"^kernel:\s*(\S+)", txt, re.M)
+        m_h = re.search(r"^source_sha256_16:\s*(\S+)", txt, re.M)
+        m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
+        if m_k and m_h and m_t and m_k.group(1) == kernel and m_h.group(1) == digest:
+            return float(m_t.group(1)), digest
+    return None, digest
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    Q = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        rows = []
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 10:
+                continue
+            if self.bus_id and self.bus_id[-12:] not in f[1].lower():
+                continue
+            rows.append(f)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        pw = [float(r[4]) for r in rows if re.match(r"^[0-9.]+$", r[4])]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+def oracle_sample(w, seconds, threads=0, start=0, fixed_n=None):
+    """Time the FP64 oracle on consecutive query positions; returns (rows/s, n_positions, secs, cores)."""
+    from oracle import oracle
+    n = fixed_n
+    if n is None:
+        n = 16
+        while True:
+            idx = (start + np.arange(n)) % w.n_q
+            t0 = time.perf_counter()
+            oracle.attn_ref_workload(w, q_index=idx.astype(np.int32), n_threads=threads)
+            dt = time.perf_counter() - t0
+            if dt >= 0.5 or n >= w.n_q:
+                break
+            n *= 4
+        n = int(min(w.n_q, max(n, round(n * seconds / max(dt, 1e-6)))))
+    idx = (start + np.arange(n)) % w.n_q
+    t0 = time.perf_counter()
+    oracle.attn_ref_workload(w, q_index=idx.astype(np.int32), n_threads=threads)
+    dt = time.perf_counter() - t0
+    return n * w.n_heads / dt, n, dt, oracle.max_threads() if threads <= 0 else threads
+
+
+def run_reference(args):
+    """Reference arm: the FP64 CPU oracle, as it stands, on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from sparse_selected_cell_gb300 import gen
+    w = gen.make(CONFIG_ID)
+    n_steps = args.steps + args.warmup
+    # size each step's sample so the whole run stays within about two minutes
+    rate, n, dt, cores = oracle_sample(w, 0.5)
+    per_step = max(1, int(n * min(1.0, 110.0 / n_steps) / max(dt, 1e-3)))
+    per_step = min(per_step, w.n_q)
+    rows, secs = 0, 0.0
+    for s in range(n_steps):
+        r, nn, t, cores = oracle_sample(w, 0, start=s * per_step, fixed_n=per_step)
+        if s >= args.warmup:
+            rows += nn * w.n_heads
+            secs += t
+    value = rows / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(w), "oracle": "FP64 CPU oracle (OpenMP), per-position lists"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} consecutive query positions (all {w.n_heads} heads) per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from sparse_selected_cell_gb300 import build as qbuild
+    from sparse_selected_cell_gb300 import gen, qsa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        qbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    qsa.lib()
+
+    # every rank runs its own independent chunk of the same shape (weak scaling)
+    w = gen.make(CONFIG_ID, seed=gen.CONFIGS[CONFIG_ID]["seed"] + 1000 * rank)
+    d = qsa.to_device(w, dev)
+    stream = torch.cuda.current_stream()
+    ws = torch.empty(qsa.workspace_bytes(w.n_q), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((w.n_q, w.n_heads, 128), dtype=torch.float32, device=dev)
+    n_groups = w.n_groups
+    stride = gen.UNION_STRIDE
+    cells_b = n_groups * stride * 4
+    mask_off = (cells_b + 255) // 256 * 256
+    cnt_off = mask_off + (n_groups * stride + 255) // 256 * 256
+    ucell = ws[:cells_b].view(torch.int32).view(n_groups, stride)
+    umask = ws[mask_off:mask_off + n_groups * stride].view(n_groups, stride)
+    ucount = ws[cnt_off:cnt_off + n_groups * 4].view(torch.int32)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        qsa.union_build(d["sel"], d["sel_count"], stride, out=(ucell, umask, ucount), dev_status=status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        qsa.union_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"], ucell, umask,
+                       ucount, out=out, variant=args.variant, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
+    alg = algorithmic(w, ucount.cpu().numpy())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(bus) as clk:
+        t0.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    union_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    rows_per_step = w.n_q * w.n_heads
+    value = world * rows_per_step * args.steps / (total_ms / 1e3)
+
+    # end to end through the public call: pinned host inputs in, host output back, every step
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dd = {k: torch.empty_like(v) for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dd[k].copy_(v, non_blocking=True)
+        qsa.prompt_attn(dd["q"], dd["k_pool"], dd["v_pool"], dd["k_scale"], dd["v_scale"], dd["page_table"],
+                        dd["sel"], dd["sel_count"], out=out, workspace=ws, variant=args.variant, dev_status=status,
+                        stream=stream)
+        host_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_value = world * rows_per_step * args.e2e_steps / (e2e_ms / 1e3)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
+
+    if rank == 0:
+        hbm, bf16, bf16_sus, src = peaks()
+        attn_avg = sum(attn_ms) / len(attn_ms)
+        achieved = alg["bytes"] / (attn_avg / 1e3) / 1e9
+        tflops = alg["flops"] / (attn_avg / 1e3) / 1e12
+        t_hbm = alg["bytes"] / (hbm * 1e9) * 1e3
+        t_tc = alg["flops"] / (bf16_sus * 1e12) * 1e3
+        resolved = args.variant or qsa.default_variant()
+        kernel = "attn_tc_kernel" if resolved == qsa.ATTN_TCGEN05 else "attn_mma_kernel"
+        srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in
+                (("attn_tc.cu",) if kernel == "attn_tc_kernel" else ("attn_mma.cu",)) + ("qsa_common.cuh",)]
+        traffic, digest = read_traffic(kernel, srcs)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_desc(w), "l2": "inputs larger than L2: %.0f MB read + %.0f MB written per step"
+                       % ((sum(v.numel() * v.element_size() for v in d.values())) / 1e6, out.numel() * 4 / 1e6),
+                       "mean_union_cells": round(alg["mean_union"], 1), "union_ratio": round(alg["union_ratio"], 3),
+                       "variant": {1: "tcgen05", 2: "mma.sync"}[resolved], "parallelism": f"dp{world}"},
+            "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "kernel": kernel,
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": traffic, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg["bytes"], "flops_per_launch": alg["flops"],
+                         "attn_ms": attn_avg, "tflops": tflops, "tensor_frac_sustained": tflops / bf16_sus,
+                         "roofline_ms": max(t_hbm, t_tc), "union_build_ms": sum(union_ms) / len(union_ms),
+                         "source_sha256_16": digest},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            rate, n, dt, cores = oracle_sample(w, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": f"{n} consecutive query positions x {w.n_heads} heads of the same "
+                                              f"chunk ({dt:.1f} s, FP64, OpenMP)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

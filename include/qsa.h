@@ -1,0 +1,135 @@
+/*
+ * qsa.h -- C ABI of libqsa.so: selected-cell (QSA union) prompt attention over a
+ * paged INT8 KV cache, on GB300 (sm_103a).
+ *
+ * Source: "sycl: prompt attention over 8-query selection unions on XMX" (Strata
+ * PR #2808).  Section Summary: every prompt position attends only to its own
+ * sorted selection of at most 2,051 K/V cells; for every 8 neighbouring
+ * positions a first kernel builds the sorted union of their selections with each
+ * cell marked by the positions that chose it, and a second kernel dequantises the
+ * INT8 K/V of 64-cell chunks of that union once and runs S = Q K^T and O += P V
+ * for all 96 rows (8 positions x 12 heads) with FP32 sums, setting a cell to
+ * -inf for the positions that did not select it.  Section Extra Notes: a union
+ * cell is an int32 with its 8-position mask in a separate byte; non-resident
+ * pages are masked.  Section "What changed": the entry point carries the prompt
+ * attention contract (query, paged K/V and scales, page table, per-position
+ * selection lists and counts).
+ *
+ * Conventions shared by every entry point below
+ *   - Device pointers point to CUDA global memory of the current device; host
+ *     pointers are marked "host".  The caller owns all memory; the library
+ *     allocates nothing, keeps no state between calls and never synchronises.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued on it; the call returns before it runs.
+ *   - Shapes are fixed by the method: head dim d = 128, 12 query heads per KV
+ *     head, 64-cell pages, groups of 8 consecutive queries starting at query 0
+ *     (the last group may be ragged).
+ *   - Layouts (row-major, no padding unless a stride is given):
+ *       q          bf16  [n_q][n_kv*12][128]
+ *       k_pool     int8  [n_ppages][n_kv][64][128]      (one KV head's page = 8 KB)
+ *       v_pool     int8  [n_ppages][n_kv][64][128]
+ *       k_scale    fp16  [n_ppages][n_kv][64]           per-cell per-KV-head scale
+ *       v_scale    fp16  [n_ppages][n_kv][64]
+ *       page_table int32 [n_lpages]   physical page of logical page c>>6; < 0 = not resident
+ *       sel        int32 [n_q][sel_stride]   strictly increasing cell ids >= 0
+ *       sel_count  int32 [n_q]               0 <= count <= sel_stride
+ *       union_cells int32 [n_groups][union_stride], union_mask uint8 [..], union_count int32 [n_groups]
+ *       out        fp32  [n_q][n_kv*12][128]
+ *     with n_groups = ceil(n_q / 8).  K/V value of cell c for KV head h is
+ *     int8 * scale at [page_table[c>>6]][h][c&63]; query head i uses KV head i/12.
+ *   - bf16 / fp16 tensors are passed as uint16_t bit patterns.
+ *   - Pointers to q, k_pool, v_pool and out must be 16-byte aligned.
+ *   - Errors: a non-zero qsa_status is returned before anything is enqueued when
+ *     an argument is invalid; QSA_ERR_CUDA reports a launch failure.  Problems that
+ *     only the device can see (a bad count, cell or page-table entry, a union that
+ *     does not fit, a device wait that ran out) never cause an out-of-bounds
+ *     access: the offending cell is masked or the count clamped, and the matching
+ *     QSA_DEV_* bit is OR-ed into *dev_status when dev_status is not NULL.
+ */
+#ifndef QSA_H
+#define QSA_H
+#include <stddef.h>
+#include <stdint.h>
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_ARG = 1,          /* null pointer, negative size, bad alignment or stride */
+    QSA_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels are built for */
+    QSA_ERR_CAPACITY = 3,     /* workspace too small */
+    QSA_ERR_CUDA = 4,         /* a CUDA launch or device query failed */
+    QSA_ERR_DEVICE_CHECK = 5  /* reserved for callers decoding *dev_status */
+} qsa_status;
+
+/* Bits OR-ed into the optional device status word (int32 in device memory). */
+enum {
+    QSA_DEV_BAD_SEL_COUNT = 1,     /* a selection count outside [0, sel_stride] (clamped) */
+    QSA_DEV_UNION_OVERFLOW = 2,    /* a union longer than union_stride (truncated) */
+    QSA_DEV_BAD_CELL = 4,          /* a cell < 0 or on a page >= n_lpages (masked) */
+    QSA_DEV_BAD_PAGE = 8,          /* a page-table entry >= n_ppages (masked) */
+    QSA_DEV_BAD_UNION_COUNT = 16,  /* a union count outside [0, union_stride] (clamped) */
+    QSA_DEV_WAIT_TIMEOUT = 32      /* a pipelined kernel gave up waiting; its output is invalid */
+};
+
+/* Attention kernel variants (all sm_103a).  QSA_ATTN_DEFAULT picks the fastest. */
+enum {
+    QSA_ATTN_DEFAULT = 0,
+    QSA_ATTN_TCGEN05 = 1,   /* tcgen05.mma with TMEM accumulators, warp-specialised pipeline */
+    QSA_ATTN_MMA_SYNC = 2   /* warp-level mma.sync m16n8k16 (legacy tensor path, for comparison) */
+};
+
+/* The variant QSA_ATTN_DEFAULT resolves to in this build (QSA_ATTN_TCGEN05 or QSA_ATTN_MMA_SYNC). */
+int qsa_attn_default_variant(void);
+
+/* Human-readable name of a qsa_status value.  Never NULL. */
+const char* qsa_status_str(int status);
+
+/* Bytes of one workspace holding the union arrays for n_q queries:
+ * union_cells, then union_mask, then union_count, each 256-byte aligned.
+ * Returns 0 for n_q < 0 or union_stride <= 0. */
+size_t qsa_union_workspace_bytes(int32_t n_q, int32_t union_stride);
+
+/* Union build (first kernel).  For each group g of up to 8 consecutive queries:
+ * union_cells[g][0:union_count[g]] = the sorted set union of their selection lists,
+ * union_mask[g][u] bit j = query 8g+j selected union_cells[g][u] (bits of absent
+ * ragged queries are 0).  Entries past union_count[g] are left unspecified.
+ * Bit-exact and deterministic (no order-dependent atomics).
+ * Requires union_stride % 64 == 0 and sel_stride >= 1; union_stride >= 8*sel_stride
+ * guarantees that every union fits.  n_q == 0 returns QSA_OK with no launch. */
+int qsa_union_build(const int32_t* sel, const int32_t* sel_count, int32_t n_q, int32_t sel_stride,
+                    int32_t* union_cells, uint8_t* union_mask, int32_t* union_count,
+                    int32_t union_stride, int32_t* dev_status, void* stream);
+
+/* Union attention (second kernel).  For query i (group g = i/8, j = i%8) and
+ * query head hq: out[i][hq][:] = sum over union cells c with bit j of the mask set
+ * and a resident page of softmax(q . k_c * sm_scale) * v_c, with k_c, v_c the
+ * dequantised K/V of KV head hq/12; zeros when no such cell exists.  One CTA per
+ * (group, KV head) covers 96 rows; K/V chunks of 64 union cells are gathered
+ * through the page table and dequantised to BF16 once; the products run on
+ * tensor cores with FP32 accumulation.  Typically sm_scale = 1/sqrt(128).
+ * Tolerance against an FP64 evaluation: BF16 rounding of Q, K, V and P.
+ * `variant` is one of the QSA_ATTN_* values.  n_q == 0 returns QSA_OK. */
+int qsa_union_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
+                   const uint16_t* k_scale, const uint16_t* v_scale,
+                   const int32_t* page_table, int32_t n_lpages, int32_t n_ppages, int32_t n_kv,
+                   const int32_t* union_cells, const uint8_t* union_mask, const int32_t* union_count,
+                   int32_t union_stride, int32_t n_q, float sm_scale, float* out,
+                   int32_t variant, int32_t* dev_status, void* stream);
+
+/* Whole prompt-attention step: qsa_union_build into `workspace` (device memory
+ * of at least qsa_union_workspace_bytes(n_q, union_stride) bytes, 256-byte
+ * aligned, owned by the caller) followed by qsa_union_attn, both on `stream`.
+ * Returns QSA_ERR_CAPACITY when workspace_bytes is too small. */
+int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
+                    const uint16_t* k_scale, const uint16_t* v_scale,
+                    const int32_t* page_table, int32_t n_lpages, int32_t n_ppages, int32_t n_kv,
+                    const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
+                    float sm_scale, float* out, void* workspace, size_t workspace_bytes,
+                    int32_t union_stride, int32_t variant, int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,98 @@
+// qsa_common.cuh -- constants and small device helpers shared by the sm_103a
+// kernels of libqsa.so (union build and union attention).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+constexpr int kHeadDim = 128;     // d
+constexpr int kHeadsPerKv = 12;   // grouped query heads per KV head
+constexpr int kGroup = 8;         // queries per union group
+constexpr int kRows = kGroup * kHeadsPerKv;   // 96 query-head rows per (group, KV head)
+constexpr int kPage = 64;         // cells per page
+constexpr int kChunk = 64;        // union cells per dequantised chunk
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void report(int32_t* status, int bits) {
+    if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------- int8 -> bf16
+// Four signed bytes are widened to exact floats with the 2^23 trick: the byte
+// biased by 128 becomes the low mantissa bits of 2^23, and subtracting
+// 2^23 + 128 leaves the integer.  Scaling happens in FP32 and each pair is then
+// rounded to bf16x2 once (round to nearest even).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ void dequant4(uint32_t w, float scale, uint32_t& out01, uint32_t& out23) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float bias = 8388736.0f;   // 2^23 + 128
+    float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
+                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
+    float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
+                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
+    const float2 nb = make_float2(-bias, -bias);
+    const float2 s2 = make_float2(scale, scale);
+    a = __fmul2_rn(__fadd2_rn(a, nb), s2);
+    b = __fmul2_rn(__fadd2_rn(b, nb), s2);
+    out01 = pack_bf16x2(a.x, a.y);
+    out23 = pack_bf16x2(b.x, b.y);
+}
+
+// 16 int8 values -> 16 bf16 values (two 16-byte words), times `scale`.
+__device__ __forceinline__ void dequant16(uint4 raw, float scale, uint4& lo, uint4& hi) {
+    dequant4(raw.x, scale, lo.x, lo.y);
+    dequant4(raw.y, scale, lo.z, lo.w);
+    dequant4(raw.z, scale, hi.x, hi.y);
+    dequant4(raw.w, scale, hi.z, hi.w);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- launchers
+// Implemented in union_build.cu / attn_mma.cu / attn_tc.cu; called by capi.cu
+// after argument validation.  They return cudaGetLastError() of the launch.
+cudaError_t launch_union_build(const int32_t* sel, const int32_t* sel_count, int n_q, int sel_stride,
+                               int32_t* union_cells, uint8_t* union_mask, int32_t* union_count,
+                               int union_stride, int32_t* dev_status, cudaStream_t stream);
+
+struct AttnArgs {
+    const uint16_t* q;
+    const int8_t* k_pool;
+    const int8_t* v_pool;
+    const uint16_t* k_scale;
+    const uint16_t* v_scale;
+    const int32_t* page_table;
+    int n_lpages, n_ppages, n_kv;
+    const int32_t* union_cells;
+    const uint8_t* union_mask;
+    const int32_t* union_count;
+    int union_stride, n_q;
+    float sm_scale;
+    float* out;
+    int32_t* dev_status;
+};
+
+cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
+
+}  // namespace qsa

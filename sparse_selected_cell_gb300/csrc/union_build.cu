@@ -1,0 +1,181 @@
+// union_build.cu -- first kernel: per group of 8 neighbouring queries, the sorted
+// union of their selection lists with an 8-bit membership mask per cell.
+//
+// Source: "sycl: prompt attention over 8-query selection unions on XMX" (Strata
+// PR #2808), section Summary (for every 8 neighbouring positions, the sorted
+// union of their selected cells, each marked with the positions that chose it)
+// and section "What changed" (one work-group per 8 positions over a local cell
+// bitmap).  Section Extra Notes fixes the storage: int32 cell + separate mask byte.
+//
+// GB300 design: one 256-thread CTA per group.  The group's cell range is walked
+// in windows of kWindow cells held as a byte map in shared memory (byte = the
+// 8-position mask).  Each list is sorted, so its cells inside a window form one
+// contiguous index range found by binary search; each cell ORs bit j into its
+// byte (OR is order-independent, so the result is deterministic).  The window is
+// then compacted in cell order: every thread takes 16 consecutive bytes, counts
+// the non-zero ones, and a block prefix sum (warp shuffles + one shared-memory
+// pass over the 8 warp totals) gives each thread its output offset.  Output is
+// sorted by construction and bit-exact.
+#include "qsa_common.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWindow = 65536;                 // cells (= bytes of shared memory) per window
+
+__device__ __forceinline__ int lower_bound(const int32_t* __restrict__ a, int n, long long x) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if ((long long)__ldg(a + mid) < x) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int nonzero_bytes(uint32_t w) {
+    // bytes of w that are non-zero -> one bit each (bit 7 of each byte), counted
+    uint32_t t = (w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;
+    t = (t | w) & 0x80808080u;
+    return __popc(t);
+}
+
+__global__ void __launch_bounds__(kThreads)
+union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ sel_count, int n_q,
+                   int sel_stride, int32_t* __restrict__ ucell, uint8_t* __restrict__ umask,
+                   int32_t* __restrict__ ucount, int ustride, int32_t* dev_status) {
+    extern __shared__ uint4 smem_map[];                  // kWindow bytes
+    uint32_t* map32 = reinterpret_cast<uint32_t*>(smem_map);
+    __shared__ int s_cnt[kGroup];
+    __shared__ int s_first[kGroup], s_last[kGroup];
+    __shared__ int s_beg[kGroup], s_end[kGroup];
+    __shared__ int s_warp[kThreads / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = blockIdx.x;
+    const int q_begin = g * kGroup;
+    const int nj = min(kGroup, n_q - q_begin);
+    const size_t out_base = (size_t)g * ustride;
+
+    if (tid < kGroup) {
+        int c = 0, first = INT32_MAX, last = INT32_MIN;
+        if (tid < nj) {
+            c = __ldg(sel_count + q_begin + tid);
+            if (c < 0 || c > sel_stride) {
+                report(dev_status, QSA_DEV_BAD_SEL_COUNT);
+                c = c < 0 ? 0 : sel_stride;
+            }
+            if (c > 0) {
+                const int32_t* lst = sel + (size_t)(q_begin + tid) * sel_stride;
+                first = __ldg(lst);
+                last = __ldg(lst + c - 1);
+            }
+        }
+        s_cnt[tid] = c;
+        s_first[tid] = first;
+        s_last[tid] = last;
+    }
+    __syncthreads();
+    long long lo = INT32_MAX, hi = INT32_MIN;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j) {
+        if (s_cnt[j] > 0) {
+            lo = min(lo, (long long)s_first[j]);
+            hi = max(hi, (long long)s_last[j]);
+        }
+    }
+    int written = 0;   // union entries produced so far (same value in every thread)
+    for (long long w0 = lo & ~15LL; w0 <= hi; w0 += kWindow) {
+        // 1. clear the byte map of this window (only the part the window can use)
+        const long long span = min((long long)kWindow, hi - w0 + 1);
+        const int n_pieces = (int)((span + 15) >> 4);
+        for (int p = tid; p < n_pieces; p += kThreads) smem_map[p] = make_uint4(0, 0, 0, 0);
+        // 2. index range of each list inside [w0, w0 + kWindow)
+        if (tid < kGroup) {
+            int b = 0, e = 0;
+            if (s_cnt[tid] > 0) {
+                const int32_t* lst = sel + (size_t)(q_begin + tid) * sel_stride;
+                b = lower_bound(lst, s_cnt[tid], w0);
+                e = lower_bound(lst, s_cnt[tid], w0 + kWindow);
+            }
+            s_beg[tid] = b;
+            s_end[tid] = e;
+        }
+        __syncthreads();
+        // 3. mark: bit j of the byte of every cell in list j
+        for (int j = 0; j < nj; ++j) {
+            const int32_t* lst = sel + (size_t)(q_begin + j) * sel_stride;
+            const int e = s_end[j];
+            for (int t = s_beg[j] + tid; t < e; t += kThreads) {
+                const long long off = (long long)__ldg(lst + t) - w0;
+                if (off >= 0 && off < span)
+                    atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + j));
+            }
+        }
+        __syncthreads();
+        // 4. compact the window in cell order
+        for (int p0 = 0; p0 < n_pieces; p0 += kThreads) {
+            const int p = p0 + tid;
+            uint4 v = p < n_pieces ? smem_map[p] : make_uint4(0, 0, 0, 0);
+            const int n = nonzero_bytes(v.x) + nonzero_bytes(v.y) + nonzero_bytes(v.z) + nonzero_bytes(v.w);
+            int incl = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) s_warp[warp] = incl;
+            __syncthreads();
+            int before = 0, total = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const int x = s_warp[w];
+                before += w < warp ? x : 0;
+                total += x;
+            }
+            if (n > 0) {
+                int idx = written + before + incl - n;
+                const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+                const long long cell0 = w0 + (long long)p * 16;
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t m = (words[k >> 2] >> ((k & 3) * 8)) & 0xFFu;
+                    if (m) {
+                        if (idx < ustride) {
+                            ucell[out_base + idx] = (int32_t)(cell0 + k);
+                            umask[out_base + idx] = (uint8_t)m;
+                        }
+                        ++idx;
+                    }
+                }
+            }
+            written += total;
+            __syncthreads();      // s_warp is reused by the next piece round
+        }
+    }
+    if (tid == 0) {
+        if (written > ustride) {
+            report(dev_status, QSA_DEV_UNION_OVERFLOW);
+            written = ustride;
+        }
+        ucount[g] = written;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_union_build(const int32_t* sel, const int32_t* sel_count, int n_q, int sel_stride,
+                               int32_t* union_cells, uint8_t* union_mask, int32_t* union_count,
+                               int union_stride, int32_t* dev_status, cudaStream_t stream) {
+    // Per-call (and so per-device) opt-in to the 64 KB byte map.
+    cudaError_t e = cudaFuncSetAttribute(union_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWindow);
+    if (e != cudaSuccess) return e;
+    const int n_groups = (n_q + kGroup - 1) / kGroup;
+    union_build_kernel<<<n_groups, kThreads, kWindow, stream>>>(sel, sel_count, n_q, sel_stride, union_cells,
+                                                                 union_mask, union_count, union_stride,
+                                                                 dev_status);
+    return cudaGetLastError();
+}
+
+}  // namespace qsa
