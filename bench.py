@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    p.add_argument("--n-q", type=int, default=None,
+                   help="profiling only: take the last N query positions of the chunk (smaller capture)")
     return p.parse_args()
 
 
@@ -223,7 +225,7 @@ def main():
     qsa.lib()
 
     # every rank runs its own independent chunk of the same shape (weak scaling)
-    w = gen.make(CONFIG_ID, seed=gen.CONFIGS[CONFIG_ID]["seed"] + 1000 * rank)
+    w = gen.make(CONFIG_ID, seed=gen.CONFIGS[CONFIG_ID]["seed"] + 1000 * rank, n_q=args.n_q)
     d = qsa.to_device(w, dev)
     stream = torch.cuda.current_stream()
     ws = torch.empty(qsa.workspace_bytes(w.n_q), dtype=torch.uint8, device=dev)
@@ -300,22 +302,24 @@ def main():
                         stream=stream)
         host_out.copy_(out, non_blocking=True)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = float("nan")
+    if args.e2e_steps > 0:
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
     if world > 1:
         tt = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(tt.item())
-    e2e_value = world * rows_per_step * args.e2e_steps / (e2e_ms / 1e3)
+    e2e_value = world * rows_per_step * args.e2e_steps / (e2e_ms / 1e3) if args.e2e_steps > 0 else None
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
 

@@ -13,10 +13,13 @@
 //   * warps 0-1 (one thread per union entry) walk a 3-deep register pipeline:
 //     union entry -> page table -> scales, and issue 16-byte cp.async copies of
 //     the K and V rows into a double-buffered INT8 stage;
-//   * all threads dequantise the stage to BF16 (K pre-multiplied by its scale,
-//     sm_scale and log2(e); V by its scale) into XOR-swizzled shared memory;
-//   * each warp computes S = Q K^T from register-resident Q fragments, masks,
+//   * all threads dequantise the stage to BF16 into XOR-swizzled shared memory:
+//     K exactly (int8 values are BF16-exact), V times its FP16 scale;
+//   * each warp computes S = Q K^T from register-resident Q fragments, scales
+//     each score column by its K scale * sm_scale * log2(e) in FP32, masks,
 //     runs the online softmax in the exp2 domain and accumulates O += P V.
+// Keeping K exact leaves the logits free of BF16 rounding, which matters when
+// the softmax is peaked (large |q . k|).
 #include "qsa_common.cuh"
 
 namespace qsa {
@@ -196,9 +199,9 @@ attn_mma_kernel(const AttnArgs a) {
         for (int u = tid; u < 2 * kChunk * 8; u += kThreads) {
             const int kv = u >> 9, cell = (u >> 3) & 63, seg = u & 7;
             const uint4 raw = *reinterpret_cast<const uint4*>(&s.raw[st][kv][cell][seg * 16]);
-            const float sc = kv ? s.vs[st][cell] : s.ks[st][cell];
             uint4 lo, hi;
-            dequant16(raw, sc, lo, hi);
+            if (kv) dequant16(raw, s.vs[st][cell], lo, hi);
+            else int8x16_to_bf16(raw, lo, hi);
             uint8_t* base = reinterpret_cast<uint8_t*>(kv ? &s.vb[0][0] : &s.kb[0][0]);
             *reinterpret_cast<uint4*>(base + swz(cell, 2 * seg)) = lo;
             *reinterpret_cast<uint4*>(base + swz(cell, 2 * seg + 1)) = hi;
@@ -219,16 +222,17 @@ attn_mma_kernel(const AttnArgs a) {
                 mma_bf16(sc[nt], qa[2 * kk2 + 1], b2, b3);
             }
         }
-        // mask: cell c is -inf for rows whose query did not select it
+        // column scale, then mask: cell c is -inf for rows whose query did not select it
         float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
             const int c = nt * 8 + 2 * t4;
             const uint32_t mA = s.mask[st][c], mB = s.mask[st][c + 1];
-            sc[nt][0] = ((mA >> j0) & 1u) ? sc[nt][0] : -INFINITY;
-            sc[nt][1] = ((mB >> j0) & 1u) ? sc[nt][1] : -INFINITY;
-            sc[nt][2] = ((mA >> j1) & 1u) ? sc[nt][2] : -INFINITY;
-            sc[nt][3] = ((mB >> j1) & 1u) ? sc[nt][3] : -INFINITY;
+            const float2 kc = *reinterpret_cast<const float2*>(&s.ks[st][c]);
+            sc[nt][0] = ((mA >> j0) & 1u) ? sc[nt][0] * kc.x : -INFINITY;
+            sc[nt][1] = ((mB >> j0) & 1u) ? sc[nt][1] * kc.y : -INFINITY;
+            sc[nt][2] = ((mA >> j1) & 1u) ? sc[nt][2] * kc.x : -INFINITY;
+            sc[nt][3] = ((mB >> j1) & 1u) ? sc[nt][3] * kc.y : -INFINITY;
             mx0 = fmaxf(mx0, fmaxf(sc[nt][0], sc[nt][1]));
             mx1 = fmaxf(mx1, fmaxf(sc[nt][2], sc[nt][3]));
         }

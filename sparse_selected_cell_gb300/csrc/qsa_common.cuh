@@ -50,6 +50,31 @@ __device__ __forceinline__ void dequant4(uint32_t w, float scale, uint32_t& out0
     out23 = pack_bf16x2(b.x, b.y);
 }
 
+// Exact int8 -> bf16 (|x| <= 128 fits bf16's 8-bit significand).  Each byte b
+// sits in the low byte of a 16-bit lane whose high byte is 0x43: keeping b's low
+// 7 bits gives the bf16 value 128 + (b & 127); keeping only b's bit 7 gives 128
+// or 256 (that bit lands on the exponent's lowest bit).  Their bf16 difference is
+// the two's-complement value of b, computed exactly.
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ void int8x4_to_bf16(uint32_t w, uint32_t& out01, uint32_t& out23) {
+    const uint32_t l01 = __byte_perm(w, 0x4343u, 0x5140);   // [b0, 0x43, b1, 0x43]
+    const uint32_t l23 = __byte_perm(w, 0x4343u, 0x5342);   // [b2, 0x43, b3, 0x43]
+    out01 = bf16x2_sub(l01 & 0xFF7FFF7Fu, l01 & 0xFF80FF80u);
+    out23 = bf16x2_sub(l23 & 0xFF7FFF7Fu, l23 & 0xFF80FF80u);
+}
+
+__device__ __forceinline__ void int8x16_to_bf16(uint4 raw, uint4& lo, uint4& hi) {
+    int8x4_to_bf16(raw.x, lo.x, lo.y);
+    int8x4_to_bf16(raw.y, lo.z, lo.w);
+    int8x4_to_bf16(raw.z, hi.x, hi.y);
+    int8x4_to_bf16(raw.w, hi.z, hi.w);
+}
+
 // 16 int8 values -> 16 bf16 values (two 16-byte words), times `scale`.
 __device__ __forceinline__ void dequant16(uint4 raw, float scale, uint4& lo, uint4& hi) {
     dequant4(raw.x, scale, lo.x, lo.y);
