@@ -15,7 +15,7 @@ from sparse_selected_cell_gb300 import gen
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [2]   # QSA_ATTN_MMA_SYNC (the tcgen05 variant joins once it lands)
+VARIANTS = [1, 2]   # QSA_ATTN_TCGEN05, QSA_ATTN_MMA_SYNC
 
 
 @pytest.fixture(scope="module")
