@@ -55,7 +55,7 @@ int check_attn_args(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
 
 extern "C" {
 
-int qsa_attn_default_variant(void) { return QSA_ATTN_MMA_SYNC; }
+int qsa_attn_default_variant(void) { return QSA_ATTN_TCGEN05; }
 
 const char* qsa_status_str(int status) {
     switch (status) {

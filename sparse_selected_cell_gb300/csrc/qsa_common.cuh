@@ -83,6 +83,12 @@ __device__ __forceinline__ void dequant16(uint4 raw, float scale, uint4& lo, uin
     dequant4(raw.w, scale, hi.z, hi.w);
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -111,7 +111,8 @@ def test_special_cases(qsa, workload, variant):
     vs = np.full_like(w.v_scale, np.float16(0.03125)).view(np.int16)
     got, st = run_gpu(qsa, w, variant, v_pool=vp, v_scale=vs)
     for h in range(w.n_heads):
-        np.testing.assert_allclose(got[:, h], [5, -9, 33, -100][h // 12] * 0.03125, rtol=2e-4)  # FP32 sums of ~2k weights
+        # exact up to the BF16 rounding of the weights that enter P V (relative 2^-9)
+        np.testing.assert_allclose(got[:, h], [5, -9, 33, -100][h // 12] * 0.03125, rtol=3e-3)
     # empty selections -> zeros, neighbours unaffected
     cnt = w.sel_count.copy()
     cnt[[0, 9, 63]] = 0
