@@ -129,6 +129,38 @@ int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     float sm_scale, float* out, void* workspace, size_t workspace_bytes,
                     int32_t union_stride, int32_t variant, int32_t* dev_status, void* stream);
 
+/* Bytes of the static device scratch behind qsa_prompt_attn_static (32 MiB):
+ * room for n_q <= 3256 queries at union_stride 16448, more at smaller strides. */
+#define QSA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* qsa_prompt_attn without a workspace argument and without any allocation.
+ * The method's description has no counterpart of this call: it exists for
+ * callers that cannot hand over device memory -- a plain C host with no device
+ * allocator of its own, for which cudaMalloc / cudaFree around each step would
+ * synchronise the device, or a caller inside a framework whose allocator it
+ * cannot reach.  The union arrays go to a scratch of QSA_STATIC_SCRATCH_BYTES
+ * in this library's static device memory (one per device), and the result is
+ * that of qsa_prompt_attn on a workspace of that size.
+ *   - Arguments, layouts and ownership are those of qsa_prompt_attn; the
+ *     stream must belong to the current device.
+ *   - Returns QSA_ERR_CAPACITY, before any CUDA call, when
+ *     qsa_union_workspace_bytes(n_q, union_stride) > QSA_STATIC_SCRATCH_BYTES;
+ *     QSA_ERR_CUDA when the scratch's address cannot be resolved.
+ *   - The first call on each device resolves the scratch's address with
+ *     cudaGetSymbolAddress (this may load the library's device code on that
+ *     device); make that first call before any stream capture begins.
+ *   - Nothing in the scratch must start at zero (the union build writes all
+ *     that the attention kernel reads), so no call clears it.
+ *   - All calls on one device share the one scratch: two calls whose work can
+ *     overlap on the device (different streams, or different host threads
+ *     without ordering between their streams) race on it.  Order them. */
+int qsa_prompt_attn_static(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
+                           const uint16_t* k_scale, const uint16_t* v_scale,
+                           const int32_t* page_table, int32_t n_lpages, int32_t n_ppages, int32_t n_kv,
+                           const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
+                           float sm_scale, float* out, int32_t union_stride, int32_t variant,
+                           int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
