@@ -36,6 +36,29 @@ UNIT = "query-head rows/s"
 CONFIG_ID = 4
 
 
+def rank_seed(rank: int) -> int:
+    """Seed of rank `rank`'s chunk: every rank runs its own independent chunk of the
+    same shape (weak scaling; the path has no exchange step between ranks)."""
+    from sparse_selected_cell_gb300 import gen
+    return gen.CONFIGS[CONFIG_ID]["seed"] + 1000 * rank
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The slowest rank's figure (timing rule); the identity on a single process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(world: int, rows_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: the rows all ranks processed over the slowest rank's time."""
+    return world * rows_per_step * steps / (ms / 1e3)
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -225,7 +248,7 @@ def main():
     qsa.lib()
 
     # every rank runs its own independent chunk of the same shape (weak scaling)
-    w = gen.make(CONFIG_ID, seed=gen.CONFIGS[CONFIG_ID]["seed"] + 1000 * rank, n_q=args.n_q)
+    w = gen.make(CONFIG_ID, seed=rank_seed(rank), n_q=args.n_q)
     d = qsa.to_device(w, dev)
     stream = torch.cuda.current_stream()
     ws = torch.empty(qsa.workspace_bytes(w.n_q), dtype=torch.uint8, device=dev)
@@ -280,12 +303,9 @@ def main():
     total_ms = t0.elapsed_time(t1)
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     union_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dev)
     rows_per_step = w.n_q * w.n_heads
-    value = world * rows_per_step * args.steps / (total_ms / 1e3)
+    value = job_rows_per_s(world, rows_per_step, args.steps, total_ms)
 
     # end to end through the public call: pinned host inputs in, host output back, every step
     host = {k: v.cpu().pin_memory() for k, v in d.items()}
@@ -315,11 +335,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_value = world * rows_per_step * args.e2e_steps / (e2e_ms / 1e3) if args.e2e_steps > 0 else None
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = job_rows_per_s(world, rows_per_step, args.e2e_steps, e2e_ms) if args.e2e_steps > 0 else None
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
 
@@ -333,7 +350,7 @@ def main():
         resolved = args.variant or qsa.default_variant()
         kernel = "attn_tc_kernel" if resolved == qsa.ATTN_TCGEN05 else "attn_mma_kernel"
         srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in
-                (("attn_tc.cu",) if kernel == "attn_tc_kernel" else ("attn_mma.cu",)) + ("qsa_common.cuh",)]
+                (("attn_tc.cu", "tc_ptx.cuh") if kernel == "attn_tc_kernel" else ("attn_mma.cu",)) + ("qsa_common.cuh",)]
         traffic, digest = read_traffic(kernel, srcs)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

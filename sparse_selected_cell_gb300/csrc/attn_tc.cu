@@ -21,8 +21,8 @@
 //              2^8, and O is rescaled in TMEM only then), writes P as BF16 into
 //              the S columns, and finally divides O by the FP32 sum of the
 //              weights and stores it.
-//   warp 3     producer: union entries -> page table -> per-chunk tables in a
-//              4-deep ring shared by both tiles (pool row of each cell, scales of
+//   warp 3     producer: union entries -> page table -> per-chunk tables in an
+//              8-deep ring shared by both tiles (pool row of each cell, scales of
 //              both KV heads, one 64-bit selection mask per query built with warp
 //              ballots), three chunks of loads in flight.  Also zeroes the Q
 //              tiles' pad rows.
