@@ -68,7 +68,11 @@ constexpr int kNB = 2;                     // BF16 operand buffers per tile
 constexpr uint32_t kTmemCols = 256 * kTiles;
 constexpr uint32_t kTileCols = 256;        // TMEM columns per tile
 constexpr uint32_t kColS = 0, kColO = 128;  // S buffer sb at kColS + 64 * sb
-constexpr float kRescaleLog2 = 8.f;        // lazy rescale threshold (exp2 domain)
+// Lazy rescale threshold (exp2 domain): the running max only moves, and O is
+// only rescaled, when a score exceeds it by more than 2^32 in p.  P then stays
+// below 2^32 (BF16 holds it), O and l below ~1e23 (FP32 holds them), and BF16 /
+// FP32 rounding is relative, so a stale max costs no accuracy.
+constexpr float kRescaleLog2 = 32.f;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 struct RawTab {
@@ -118,6 +122,10 @@ __device__ __forceinline__ bool wait_addr(const Ctx& c, uint32_t addr, uint32_t 
 }
 
 // ------------------------------------------------------------------ producer
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 struct Entries {
     int cell[2], mask[2];
     bool present[2];
@@ -213,6 +221,16 @@ __device__ void producer_role(const Ctx& c, int lane) {
         load_pages(c, e2, pg2);
         pool_rows(c, e1, pg1, r1);
         const Scales s1 = load_scales(c, r1);
+        // the loaders gather chunk i+1 several chunks from now: pull its rows into L2
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+            for (int u = 0; u < kTiles; ++u)
+                if (r1[k] >= 0 && u < c.n_tiles) {
+                    const size_t off = (size_t)(r1[k] + u * kPage) * kHeadDim;
+                    prefetch_l2(c.a->k_pool + off);
+                    prefetch_l2(c.a->v_pool + off);
+                }
         if (!wait_addr(c, bar(c, BAR_TAB_EMPTY + ts), ((i / kNS) & 1) ^ 1)) break;
         RawTab* T = raw_tab(c, ts);
 #pragma unroll
