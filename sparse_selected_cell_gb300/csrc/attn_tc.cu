@@ -268,22 +268,31 @@ __device__ void producer_role(const Ctx& c, int lane) {
 }
 
 // ------------------------------------------------------------------ loaders / converters
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+
+// Thread ct of the loader group owns rows (ct >> 3) + 16k, k = 0..3.  Lane i =
+// ct & 7 of each 8-lane group takes bytes [8i, 8i+8) and [64+8i, 64+8i+8) of a
+// row: BF16 columns 8i..8i+7 of the tile's first and of its second 64-column
+// half.  So each 16-byte store of the group fills exactly one 128-byte row of
+// one half (one shared-memory wavefront, conflict-free under the swizzle).
+constexpr int kRowsPerThread = kChunk * 8 / kConvThreads;
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
 
-// Thread ct of the loader group owns rows (ct >> 3) + 16k, k = 0..3, 16-byte
-// segment ct & 7, of both K and V.
-constexpr int kRowsPerThread = kChunk * 8 / kConvThreads;
 __device__ __forceinline__ void load_rows(const int8_t* pool, const RawTab* T, int ct, uint4 (&x)[kRowsPerThread]) {
-    const int seg = ct & 7;
+    const int i = ct & 7;
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
         const int r = T->row[(ct >> 3) + (kConvThreads / 8) * k];
-        x[k] = r >= 0 ? ldg_stream(pool + (size_t)r * kHeadDim + seg * 16) : make_uint4(0, 0, 0, 0);
+        if (r >= 0) {
+            const int8_t* src = pool + (size_t)r * kHeadDim + 8 * i;
+            const uint2 a = ldg_stream8(src), b = ldg_stream8(src + 64);
+            x[k] = make_uint4(a.x, a.y, b.x, b.y);
+        } else {
+            x[k] = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
@@ -295,17 +304,18 @@ __device__ __forceinline__ bool prefetch_k(const Ctx& c, int ct, int i, uint4 (&
     return true;
 }
 
-__device__ __forceinline__ void tile_offsets(int ct, int k, uint32_t& o_a, uint32_t& o_b, bool& odd_first) {
-    // Segments 0-3 fill the first 64 columns, 4-7 the second (8 KB apart, same
-    // banks); the upper four store their odd 16-byte chunk first, so each
-    // quarter-warp store covers eight distinct bank groups.
-    const int seg = ct & 7, row = (ct >> 3) + (kConvThreads / 8) * k;
-    odd_first = (seg & 4) != 0;
-    const uint32_t q = (uint32_t)(seg & 3) * 2, x = (uint32_t)(row & 7);
-    const uint32_t tile = (uint32_t)(seg >> 2) * (kTileBytes / 2) + (uint32_t)row * 128;
-    const uint32_t o_lo = tile + ((q ^ x) << 4), o_hi = tile + (((q + 1) ^ x) << 4);
-    o_a = odd_first ? o_hi : o_lo;
-    o_b = odd_first ? o_lo : o_hi;
+// Converts the thread's 2 x 8 bytes of row k and stores them as BF16 into both
+// halves of the 128-byte-swizzled tile at `tile`.
+__device__ __forceinline__ void store_row(uint8_t* tile, int ct, int k, uint4 x) {
+    const int i = ct & 7, row = (ct >> 3) + (kConvThreads / 8) * k;
+    const uint32_t off = (uint32_t)row * 128 + ((uint32_t)(i ^ (row & 7)) << 4);
+    uint4 lo, hi;
+    int8x4_to_bf16(x.x, lo.x, lo.y);
+    int8x4_to_bf16(x.y, lo.z, lo.w);
+    int8x4_to_bf16(x.z, hi.x, hi.y);
+    int8x4_to_bf16(x.w, hi.z, hi.w);
+    *reinterpret_cast<uint4*>(tile + off) = lo;
+    *reinterpret_cast<uint4*>(tile + kTileBytes / 2 + off) = hi;
 }
 
 // Chunk i: its K rows are in registers.  Issue its V loads, convert K into the
@@ -322,30 +332,14 @@ __device__ __forceinline__ bool convert_chunk(const Ctx& c, int ct, int i, const
     load_rows(c.a->v_pool, T, ct, vx);
     if (!wait_addr(c, bar(c, BAR_K_EMPTY + b), par)) return false;
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-        uint32_t o_a, o_b;
-        bool odd_first;
-        tile_offsets(ct, k, o_a, o_b, odd_first);
-        uint4 lo, hi;
-        int8x16_to_bf16(kx[k], lo, hi);
-        *reinterpret_cast<uint4*>(kb + o_a) = odd_first ? hi : lo;
-        *reinterpret_cast<uint4*>(kb + o_b) = odd_first ? lo : hi;
-    }
+    for (int k = 0; k < kRowsPerThread; ++k) store_row(kb, ct, k, kx[k]);
     tc::fence_proxy_async();
     __syncwarp();
     if ((ct & 31) == 0) tc::mbar_arrive(bar(c, BAR_K_FULL + b));
     if (!prefetch_k(c, ct, i + 1, kn)) return false;
     if (!wait_addr(c, bar(c, BAR_V_EMPTY + b), par)) return false;
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-        uint32_t o_a, o_b;
-        bool odd_first;
-        tile_offsets(ct, k, o_a, o_b, odd_first);
-        uint4 lo, hi;
-        int8x16_to_bf16(vx[k], lo, hi);
-        *reinterpret_cast<uint4*>(vb + o_a) = odd_first ? hi : lo;
-        *reinterpret_cast<uint4*>(vb + o_b) = odd_first ? lo : hi;
-    }
+    for (int k = 0; k < kRowsPerThread; ++k) store_row(vb, ct, k, vx[k]);
     tc::fence_proxy_async();
     __syncwarp();
     if ((ct & 31) == 0) {
