@@ -144,14 +144,32 @@ struct Entries {
     bool present[2];
 };
 
-__device__ __forceinline__ Entries load_entries(const Ctx& c, int chunk, int lane) {
+// Chunk placement.  `lead` is the index of the first page-aligned union cell
+// after entry 0 among entries 1..63 (0 if there is none).  Chunk c holds union
+// positions p = lead + 64c + slot, slot = 0..63; a position past the end wraps
+// to entry p - U when that is one of the `lead` entries before it, and is
+// empty otherwise.  So every union entry sits in exactly one slot and the chunk
+// count stays ceil(U / 64); when the union is a few loose cells (such as sink
+// cells 0-2) followed by whole 64-cell pages, every chunk but the last is one
+// whole page, and each query selects all of such a chunk or none of it.
+__device__ __forceinline__ int union_lead(const Ctx& c, int lane) {
+    const int32_t* ucell = c.a->union_cells + (size_t)c.g * c.a->union_stride;
+    const uint32_t b0 =
+        __ballot_sync(0xffffffffu, lane >= 1 && lane < c.U && (__ldg(ucell + lane) & (kPage - 1)) == 0);
+    if (b0) return __ffs(b0) - 1;
+    const uint32_t b1 = __ballot_sync(0xffffffffu, 32 + lane < c.U && (__ldg(ucell + 32 + lane) & (kPage - 1)) == 0);
+    return b1 ? 31 + __ffs(b1) : 0;
+}
+
+__device__ __forceinline__ Entries load_entries(const Ctx& c, int lead, int chunk, int lane) {
     Entries e;
     const int32_t* ucell = c.a->union_cells + (size_t)c.g * c.a->union_stride;
     const uint8_t* umask = c.a->union_mask + (size_t)c.g * c.a->union_stride;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        const int u = chunk * kChunk + lane + 32 * k;
-        e.present[k] = chunk < c.n_chunks && u < c.U;
+        const int p = lead + chunk * kChunk + lane + 32 * k;
+        const int u = p < c.U ? p : (p - c.U < lead ? p - c.U : -1);
+        e.present[k] = chunk < c.n_chunks && u >= 0;
         e.cell[k] = e.present[k] ? __ldg(ucell + u) : 0;
         e.mask[k] = e.present[k] ? __ldg(umask + u) : 0;
     }
@@ -217,7 +235,9 @@ __device__ void producer_role(const Ctx& c, int lane) {
     __syncwarp();
     if (lane == 0) tc::mbar_arrive(bar(c, BAR_Q_READY));
     if (c.n_chunks == 0) return;
-    Entries e0 = load_entries(c, 0, lane), e1 = load_entries(c, 1, lane), e2 = load_entries(c, 2, lane);
+    const int lead = union_lead(c, lane);
+    Entries e0 = load_entries(c, lead, 0, lane), e1 = load_entries(c, lead, 1, lane),
+            e2 = load_entries(c, lead, 2, lane);
     int pg0[2], pg1[2], r0[2];
     load_pages(c, e0, pg0);
     load_pages(c, e1, pg1);
@@ -225,7 +245,7 @@ __device__ void producer_role(const Ctx& c, int lane) {
     Scales s0 = load_scales(c, r0);
     for (int i = 0; i < c.n_chunks; ++i) {
         const int ts = i % kNS;
-        const Entries e3 = load_entries(c, i + 3, lane);
+        const Entries e3 = load_entries(c, lead, i + 3, lane);
         int pg2[2], r1[2];
         load_pages(c, e2, pg2);
         pool_rows(c, e1, pg1, r1);
@@ -421,8 +441,30 @@ __device__ void mma_role(const Ctx& c) {
 
 // ------------------------------------------------------------------ softmax
 // Scale + mask 16 score columns: v = s * ks where selected, -inf elsewhere
-// (ks: the 16 columns' K scales in shared memory).
-__device__ __forceinline__ void scale_mask16(uint32_t* s, uint32_t sel, const float* ks, float& mx, float& my) {
+// (ks: the 16 columns' K scales in shared memory).  `uniform` (warp-uniform):
+// every lane selected all of the slice or none of it, so the mask is a per-lane
+// bias (0 or -inf) added in the same FMA.
+__device__ __forceinline__ void scale_mask16(uint32_t* s, uint32_t sel, bool uniform, const float* ks, float& mx,
+                                             float& my) {
+    if (uniform) {
+        const float bias = sel ? 0.f : -INFINITY;
+        const float2 b2 = make_float2(bias, bias);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+            const float4 kq = *reinterpret_cast<const float4*>(ks + 4 * c4);
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(s[4 * c4]), __uint_as_float(s[4 * c4 + 1])),
+                                        make_float2(kq.x, kq.y), b2);
+            const float2 b = __ffma2_rn(make_float2(__uint_as_float(s[4 * c4 + 2]), __uint_as_float(s[4 * c4 + 3])),
+                                        make_float2(kq.z, kq.w), b2);
+            s[4 * c4] = __float_as_uint(a.x);
+            s[4 * c4 + 1] = __float_as_uint(a.y);
+            s[4 * c4 + 2] = __float_as_uint(b.x);
+            s[4 * c4 + 3] = __float_as_uint(b.y);
+            mx = fmax3(mx, a.x, a.y);
+            my = fmax3(my, b.x, b.y);
+        }
+        return;
+    }
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
         const float4 kq = *reinterpret_cast<const float4*>(ks + 4 * c4);
@@ -505,11 +547,13 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         // A 16-column slice that none of the warp's queries selected is skipped (its P is zero).
         const uint32_t sel_lo = sel & 0xFFFFu, sel_hi = sel >> 16;
         const bool act_lo = __any_sync(0xffffffffu, sel_lo != 0), act_hi = __any_sync(0xffffffffu, sel_hi != 0);
+        const bool uni_lo = __all_sync(0xffffffffu, sel_lo == 0 || sel_lo == 0xFFFFu);
+        const bool uni_hi = __all_sync(0xffffffffu, sel_hi == 0 || sel_hi == 0xFFFFu);
         const float* ksp = &T->ks[32 * hf];
         tc::tmem_wait_ld();
         float mx = -INFINITY, my = -INFINITY;    // two chains for more ILP
-        if (act_lo) scale_mask16(&sv[0], sel_lo, ksp, mx, my);
-        if (act_hi) scale_mask16(&sv[16], sel_hi, ksp + 16, mx, my);
+        if (act_lo) scale_mask16(&sv[0], sel_lo, uni_lo, ksp, mx, my);
+        if (act_hi) scale_mask16(&sv[16], sel_hi, uni_hi, ksp + 16, mx, my);
         // swap half-chunk maxima with the partner warp, so both take the same step
         float* xb = xchg + (t & 1) * (2 * kRows);
         xb[hf * kRows + r] = fmaxf(mx, my);
