@@ -7,21 +7,25 @@
 // and section "What changed" (one work-group per 8 positions over a local cell
 // bitmap).  Section Extra Notes fixes the storage: int32 cell + separate mask byte.
 //
-// GB300 design: one 256-thread CTA per group.  The group's cell range is walked
+// GB300 design: one 512-thread CTA per group.  The group's cell range is walked
 // in windows of kWindow cells held as a byte map in shared memory (byte = the
-// 8-position mask).  Each list is sorted, so its cells inside a window form one
-// contiguous index range found by binary search; each cell ORs bit j into its
-// byte (OR is order-independent, so the result is deterministic).  The window is
-// then compacted in cell order: every thread takes 16 consecutive bytes, counts
-// the non-zero ones, and a block prefix sum (warp shuffles + one shared-memory
-// pass over the 8 warp totals) gives each thread its output offset.  Output is
-// sorted by construction and bit-exact.
+// 8-position mask); a context up to kWindow cells is one window.  Each list is
+// sorted, so its cells inside a window form one contiguous index range (found
+// by binary search only when there are several windows).  The 8 ranges are
+// marked as one flattened index space, eight loads in flight per thread before
+// their ORs of bit j into the cell's byte (OR is order-independent, so the
+// result is deterministic).  The window is then compacted in cell order: every
+// thread takes 16 consecutive bytes, counts the non-zero ones, and a block
+// prefix sum (warp shuffles + one shared-memory pass over the warp totals)
+// gives each thread its output offset.  Output is sorted by construction and
+// bit-exact.
 #include "qsa_common.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kMarkUnroll = 8;                 // list entries loaded per thread before marking
 constexpr int kWindow = 65536;                 // cells (= bytes of shared memory) per window
 
 __device__ __forceinline__ int lower_bound(const int32_t* __restrict__ a, int n, long long x) {
@@ -92,25 +96,51 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
         const int n_pieces = (int)((span + 15) >> 4);
         for (int p = tid; p < n_pieces; p += kThreads) smem_map[p] = make_uint4(0, 0, 0, 0);
         // 2. index range of each list inside [w0, w0 + kWindow)
+        const bool one_window = hi - w0 < kWindow;
         if (tid < kGroup) {
             int b = 0, e = 0;
             if (s_cnt[tid] > 0) {
-                const int32_t* lst = sel + (size_t)(q_begin + tid) * sel_stride;
-                b = lower_bound(lst, s_cnt[tid], w0);
-                e = lower_bound(lst, s_cnt[tid], w0 + kWindow);
+                if (one_window) {
+                    e = s_cnt[tid];
+                } else {
+                    const int32_t* lst = sel + (size_t)(q_begin + tid) * sel_stride;
+                    b = lower_bound(lst, s_cnt[tid], w0);
+                    e = lower_bound(lst, s_cnt[tid], w0 + kWindow);
+                }
             }
             s_beg[tid] = b;
             s_end[tid] = e;
         }
         __syncthreads();
-        // 3. mark: bit j of the byte of every cell in list j
-        for (int j = 0; j < nj; ++j) {
-            const int32_t* lst = sel + (size_t)(q_begin + j) * sel_stride;
-            const int e = s_end[j];
-            for (int t = s_beg[j] + tid; t < e; t += kThreads) {
-                const long long off = (long long)__ldg(lst + t) - w0;
-                if (off >= 0 && off < span)
-                    atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + j));
+        // 3. mark: bit j of the byte of every cell in list j; the lists' ranges
+        // are one index space, kMarkUnroll loads per thread in flight at once
+        int pre[kGroup + 1];
+        pre[0] = 0;
+#pragma unroll
+        for (int j = 0; j < kGroup; ++j) pre[j + 1] = pre[j] + (j < nj ? s_end[j] - s_beg[j] : 0);
+        const int total = pre[kGroup];
+        for (int base = 0; base < total; base += kThreads * kMarkUnroll) {
+            int cell[kMarkUnroll], jj[kMarkUnroll];
+#pragma unroll
+            for (int u = 0; u < kMarkUnroll; ++u) {
+                const int idx = base + u * kThreads + tid;
+                int j = 0, start = 0;
+#pragma unroll
+                for (int k = 1; k < kGroup; ++k)
+                    if (idx >= pre[k]) {
+                        j = k;
+                        start = pre[k];
+                    }
+                jj[u] = idx < total ? j : -1;
+                cell[u] = idx < total
+                              ? __ldg(sel + (size_t)(q_begin + j) * sel_stride + s_beg[j] + (idx - start))
+                              : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < kMarkUnroll; ++u) {
+                const long long off = (long long)cell[u] - w0;
+                if (jj[u] >= 0 && off >= 0 && off < span)
+                    atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + jj[u]));
             }
         }
         __syncthreads();
