@@ -69,6 +69,9 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
+    p.add_argument("--drift-sweep", type=str, default=None,
+                   help="comma-separated drift values: one line per value with the union ratio and the "
+                        "union-build / attention times on the benchmark workload (not the contract line)")
     p.add_argument("--n-q", type=int, default=None,
                    help="profiling only: take the last N query positions of the chunk (smaller capture)")
     return p.parse_args()
@@ -222,10 +225,54 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def drift_sweep(args):
+    """Time of the union path against the union ratio: the benchmark workload with
+    the selection drift varied (the union pages' chunk-timing table, Extra Notes)."""
+    import torch
+    from sparse_selected_cell_gb300 import build as qbuild
+    from sparse_selected_cell_gb300 import gen, qsa
+    torch.cuda.set_device(0)
+    qbuild.build()
+    for drift in (float(x) for x in args.drift_sweep.split(",")):
+        w = gen.make(CONFIG_ID, drift=drift)
+        d = qsa.to_device(w)
+        ws = torch.empty(qsa.workspace_bytes(w.n_q), dtype=torch.uint8, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        out = torch.empty((w.n_q, w.n_heads, 128), dtype=torch.float32, device="cuda")
+        G, S = w.n_groups, gen.UNION_STRIDE
+        cb = G * S * 4
+        mo = (cb + 255) // 256 * 256
+        co = mo + (G * S + 255) // 256 * 256
+        uc, um, un = ws[:cb].view(torch.int32).view(G, S), ws[mo:mo + G * S].view(G, S), ws[co:co + G * 4].view(torch.int32)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ub, at = [], []
+        for k in range(args.warmup + args.steps):
+            ev[0].record()
+            qsa.union_build(d["sel"], d["sel_count"], S, out=(uc, um, un), dev_status=st)
+            ev[1].record()
+            qsa.union_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"], uc, um, un,
+                           out=out, variant=args.variant, dev_status=st)
+            ev[2].record()
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                ub.append(ev[0].elapsed_time(ev[1]))
+                at.append(ev[1].elapsed_time(ev[2]))
+        alg = algorithmic(w, un.cpu().numpy())
+        attn = sum(at) / len(at)
+        print(json.dumps({"sweep": "drift", "drift": drift, "union_ratio": round(alg["union_ratio"], 3),
+                          "mean_union_cells": round(alg["mean_union"], 1), "union_build_ms": sum(ub) / len(ub),
+                          "attn_ms": attn, "rows_per_s": w.n_q * w.n_heads / ((attn + sum(ub) / len(ub)) / 1e3),
+                          "attn_gb_per_s": alg["bytes"] / (attn / 1e3) / 1e9,
+                          "ns_per_union_cell_head": attn * 1e6 / (alg["mean_union"] * w.n_groups * w.n_kv),
+                          "status": int(st.item())}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.drift_sweep:
+        return drift_sweep(args)
 
     import torch
     from sparse_selected_cell_gb300 import build as qbuild
