@@ -92,9 +92,11 @@ constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKb = kOffQ + kQTileBytes;
 constexpr uint32_t kOffVb = kOffKb + kNB * kTileBytes;
 constexpr uint32_t kOffRawTab = kOffVb + kNB * kTileBytes;
-// half-chunk maxima swapped by the two softmax warps of a row, by chunk parity
+// half-chunk maxima swapped by the two softmax warps of a row, by chunk parity,
+// and a third set of slots for the row sums at the end (a warp may still be
+// reading its partner's last maximum when the partner writes its sum)
 constexpr uint32_t kOffXchg = kOffRawTab + kNS * (uint32_t)sizeof(RawTab);
-constexpr uint32_t kOffBars = (kOffXchg + 2 * 2 * kRows * 4 + 7u) & ~7u;
+constexpr uint32_t kOffBars = (kOffXchg + 3 * 2 * kRows * 4 + 7u) & ~7u;
 // K and V tiles are filled and freed separately (K is free once S is done, V
 // once P V is done)
 enum { BAR_TAB_FULL = 0, BAR_TAB_EMPTY = kNS, BAR_K_FULL = 2 * kNS, BAR_K_EMPTY = BAR_K_FULL + kNB,
@@ -515,7 +517,7 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
     const bool row_ok = j < c.nj;
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const size_t row_off = ((size_t)(c.q_begin + j) * c.n_heads + (size_t)c.h * kHeadsPerKv + hq) * kHeadDim;
-    float* xchg = reinterpret_cast<float*>(c.base + kOffXchg);   // [parity][half][row]
+    float* xchg = reinterpret_cast<float*>(c.base + kOffXchg);   // [parity][half][row]; slots 2: row sums
     {   // Q row r, this warp's 64-column half -> the swizzled K-major Q tile
         uint8_t* qt = c.base + kOffQ + hf * (kQTileBytes / 2);
 #pragma unroll
@@ -614,9 +616,10 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
     }
     if (!ok) return;
     // total weight of the row: this warp's sum plus the partner's
-    xchg[hf * kRows + r] = l;
+    float* xl = xchg + 4 * kRows;
+    xl[hf * kRows + r] = l;
     pair_sync(quad);
-    const float l_tot = l + xchg[(hf ^ 1) * kRows + r];
+    const float l_tot = l + xl[(hf ^ 1) * kRows + r];
     if (!wait_addr(c, bar(c, BAR_O_DONE), 0)) return;
     tc::fence_after_sync();
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
