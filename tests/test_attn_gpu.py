@@ -161,3 +161,39 @@ def test_bad_cells_are_masked_and_reported(qsa):
         got, st = run_gpu(qsa, w, variant, sel=sel, page_table=pt)
         assert st & 4 and st & 8
         assert np.isfinite(got).all()
+
+
+def _lists(w, per_query):
+    """A selection array for workload w from per-query lists of cells (sorted, distinct)."""
+    sel = np.full_like(w.sel, -1)
+    cnt = np.zeros_like(w.sel_count)
+    for i, cells in enumerate(per_query):
+        cells = np.array(sorted(set(int(c) for c in cells)), dtype=np.int32)
+        sel[i, :len(cells)] = cells
+        cnt[i] = len(cells)
+    return sel, cnt
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_chunk_placement_edge_cases(qsa, variant):
+    """Unions whose loose leading cells wrap into the last chunk: leads of 1, 3 and
+    63 entries, unions of 5, 64 and 65 cells, no page-aligned cell at all, and
+    partly selected pages inside a chunk."""
+    w = gen.make(2, n_q=64)
+    rng = np.random.default_rng(7)
+    groups = [
+        lambda j: [0, 1, 2, 64, 65],                                      # lead 3, U = 5
+        lambda j: [0, 1, 2] + list(range(128, 128 + 61)),                 # lead 3, U = 64
+        lambda j: [0, 1, 2] + list(range(128, 128 + 62)),                 # lead 3, U = 65
+        lambda j: [5] + list(range(64, 64 + 64 + j)),                     # lead 1, a page and a partial one
+        lambda j: list(range(1, 64)) + list(range(192, 256)),             # lead 63: 63 loose cells, then a page
+        lambda j: list(range(3, 3 + 60, 3)) + list(range(1025, 1025 + 40)),  # no page-aligned cell
+        lambda j: [0] + list(range(256 + 8 * j, 320)) + list(range(640, 704)),  # per-query partial pages
+        lambda j: sorted(rng.choice(4096, size=int(rng.integers(1, 200)), replace=False).tolist()),
+    ]
+    per_query = [groups[i // 8](i % 8) for i in range(w.n_q)]
+    sel, cnt = _lists(w, per_query)
+    got, st = run_gpu(qsa, w, variant, sel=sel, sel_count=cnt)
+    assert st == 0
+    ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, sel, cnt, w.n_kv, w.sm_scale)
+    check_close(got, ref, "chunk placement edge cases")
