@@ -70,8 +70,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--drift-sweep", type=str, default=None,
-                   help="comma-separated drift values: one line per value with the union ratio and the "
-                        "union-build / attention times on the benchmark workload (not the contract line)")
+                   help="comma-separated drift values: one line per value with the union ratio, the "
+                        "union-build / attention times and the per-position path's time on the benchmark "
+                        "workload (not the contract line)")
     p.add_argument("--n-q", type=int, default=None,
                    help="profiling only: take the last N query positions of the chunk (smaller capture)")
     return p.parse_args()
@@ -257,13 +258,27 @@ def drift_sweep(args):
             if k >= args.warmup:
                 ub.append(ev[0].elapsed_time(ev[1]))
                 at.append(ev[1].elapsed_time(ev[2]))
+        # the per-position path (no union) on the same inputs: every position gathers its own cells
+        sl = []
+        for k in range(args.warmup + args.steps):
+            ev[0].record()
+            qsa.select_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"],
+                            d["sel"], d["sel_count"], out=out, dev_status=st)
+            ev[1].record()
+            torch.cuda.synchronize()
+            if k >= args.warmup:
+                sl.append(ev[0].elapsed_time(ev[1]))
         alg = algorithmic(w, un.cpu().numpy())
         attn = sum(at) / len(at)
+        sel_ms = sum(sl) / len(sl)
+        sel_bytes = int(w.sel_count.astype(np.int64).sum()) * w.n_kv * 260 + w.n_q * w.n_heads * 128 * 6
         print(json.dumps({"sweep": "drift", "drift": drift, "union_ratio": round(alg["union_ratio"], 3),
                           "mean_union_cells": round(alg["mean_union"], 1), "union_build_ms": sum(ub) / len(ub),
                           "attn_ms": attn, "rows_per_s": w.n_q * w.n_heads / ((attn + sum(ub) / len(ub)) / 1e3),
                           "attn_gb_per_s": alg["bytes"] / (attn / 1e3) / 1e9,
                           "ns_per_union_cell_head": attn * 1e6 / (alg["mean_union"] * w.n_groups * w.n_kv),
+                          "per_position_ms": sel_ms, "per_position_gb_per_s": sel_bytes / (sel_ms / 1e3) / 1e9,
+                          "union_path_speedup": sel_ms / (attn + sum(ub) / len(ub)),
                           "status": int(st.item())}), flush=True)
 
 

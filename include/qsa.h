@@ -129,6 +129,25 @@ int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     float sm_scale, float* out, void* workspace, size_t workspace_bytes,
                     int32_t union_stride, int32_t variant, int32_t* dev_status, void* stream);
 
+/* Per-position selected-cell attention without unions: out[i][hq][:] is the same
+ * softmax over query i's own resident selected cells as qsa_union_attn computes,
+ * but every position gathers its own cells ("sycl: prompt attention over 8-query
+ * selection unions on XMX", Strata PR #2808, section Summary: the prompt path's
+ * default, each position gathering its own ~2,051 cells; section Extra Notes
+ * times it against the union kernel).  It is the baseline the union path
+ * replaces, built on the warp-level tensor path (mma.sync, BF16 in, FP32 sums)
+ * with the same K/V handling as qsa_union_attn: exact BF16 K and V, K scale on
+ * the score column in FP32, V scale in P.  Arguments and layouts are those of
+ * qsa_prompt_attn (sel: [n_q][sel_stride] cells, sel_count: [n_q]); no workspace.
+ * The lists need not be sorted.  Device checks as in qsa_union_attn
+ * (QSA_DEV_BAD_SEL_COUNT, QSA_DEV_BAD_CELL, QSA_DEV_BAD_PAGE into *dev_status).
+ * n_q == 0 returns QSA_OK with no launch. */
+int qsa_select_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
+                    const uint16_t* k_scale, const uint16_t* v_scale,
+                    const int32_t* page_table, int32_t n_lpages, int32_t n_ppages, int32_t n_kv,
+                    const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
+                    float sm_scale, float* out, int32_t* dev_status, void* stream);
+
 /* Bytes of the static device scratch behind qsa_prompt_attn_static (32 MiB):
  * room for n_q <= 3256 queries at union_stride 16448, more at smaller strides. */
 #define QSA_STATIC_SCRATCH_BYTES (32u << 20)

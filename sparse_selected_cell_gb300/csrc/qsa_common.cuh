@@ -126,4 +126,23 @@ struct AttnArgs {
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
 
+// Per-position attention (no union): each query over its own selection list.
+struct SelArgs {
+    const uint16_t* q;
+    const int8_t* k_pool;
+    const int8_t* v_pool;
+    const uint16_t* k_scale;
+    const uint16_t* v_scale;
+    const int32_t* page_table;
+    int n_lpages, n_ppages, n_kv;
+    const int32_t* sel;
+    const int32_t* sel_count;
+    int sel_stride, n_q;
+    float sm_scale;
+    float* out;
+    int32_t* dev_status;
+};
+
+cudaError_t launch_select_attn(const SelArgs& a, cudaStream_t stream);
+
 }  // namespace qsa

@@ -1,0 +1,297 @@
+// select_attn.cu -- per-position selected-cell attention without unions: every
+// query position gathers its own selected cells (the baseline the union path
+// replaces).
+//
+// Source: "sycl: prompt attention over 8-query selection unions on XMX" (Strata
+// PR #2808), section Summary: the engine's default prompt path runs the decode
+// kernel, every position gathering its own ~2,051 selected K/V cells; section
+// Extra Notes times it against the union kernel at several union ratios.  The
+// result is the same per-position softmax the union path computes; here it runs
+// on the warp-level tensor path so that the comparison is between data-movement
+// strategies, not between FP32 and tensor cores.
+//
+// One warp per (query position i, KV head h): its 12 query heads are rows 0-11
+// of one m16 tile (rows 12-15 padding), Q held as A fragments in registers.  The
+// position's list is walked in steps of 16 cells:
+//   * lanes 0-15 resolve cell -> page -> pool row for the K rows, lanes 16-31 for
+//     the V rows, in a three-step register pipeline (cells two steps ahead, the
+//     page table one step ahead), and issue 16-byte cp.async copies of the rows
+//     into a double-buffered INT8 stage (16-byte chunks XOR-swizzled by cell);
+//   * the warp converts the stage exactly to BF16 tiles (|int8| <= 127 fits
+//     BF16), S = Q K^T with mma.sync m16n8k16, the K scale (times sm_scale and
+//     log2 e) multiplies each score column in FP32, unselected / masked cells
+//     are -inf, the online softmax runs in the exp2 domain with the same lazy
+//     rescale as the union kernel, P = p * (V scale) enters O += P V as BF16.
+#include "qsa_common.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kSelWarps = 4;
+constexpr int kSelThreads = 32 * kSelWarps;
+constexpr int kStep = 16;                  // cells per step
+constexpr float kSelRescaleLog2 = 32.f;    // lazy rescale threshold (exp2 domain), as in attn_tc.cu
+
+struct __align__(16) WarpSmem {
+    int8_t raw[2][2][kStep][kHeadDim];      // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   8 KB
+    uint16_t kb[kStep][kHeadDim];           // BF16 K, 256-byte rows, 16-byte chunks XOR (cell & 7)   4 KB
+    uint16_t vb[kStep][kHeadDim];           // BF16 V                                                4 KB
+    float ks[2][kStep];                     // K scale * sm_scale * log2(e); 0 for a masked cell
+    float vs[2][kStep];                     // V scale; 0 for a masked cell
+    uint32_t valid[2];                      // bit c: cell c of the step is selected and resident
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// byte offset of 16-byte chunk `chunk` of a row `cell` of `row_bytes` bytes
+__device__ __forceinline__ uint32_t swz(int cell, int chunk, int row_bytes) {
+    return (uint32_t)(cell * row_bytes + ((chunk ^ (cell & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    WarpSmem& s = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
+    const long long item = (long long)blockIdx.x * kSelWarps + warp;   // h-major: consecutive positions share cells
+    if (item >= (long long)a.n_q * a.n_kv) return;
+    const int h = (int)(item / a.n_q), i = (int)(item - (long long)h * a.n_q);
+    const int n_heads = a.n_kv * kHeadsPerKv;
+    const float kmul = a.sm_scale * kLog2e;
+
+    int cnt = __ldg(a.sel_count + i);
+    if (cnt < 0 || cnt > a.sel_stride) {
+        if (lane == 0) report(a.dev_status, QSA_DEV_BAD_SEL_COUNT);
+        cnt = cnt < 0 ? 0 : a.sel_stride;
+    }
+    const int n_steps = (cnt + kStep - 1) / kStep;
+    const int32_t* lst = a.sel + (size_t)i * a.sel_stride;
+
+    // ---- cell -> page -> row pipeline: lane l handles cell (l & 15) of a step, K (l < 16) or V (l >= 16)
+    const int slot = lane & 15, kv = lane >> 4;
+    auto load_cell = [&](int step) -> int {
+        const int u = step * kStep + slot;
+        return (step < n_steps && u < cnt) ? __ldg(lst + u) : -1;
+    };
+    auto resolve = [&](int cell) -> int {      // physical page, -1 = masked (absent, bad or not resident)
+        if (cell < 0) return -1;
+        if ((cell >> 6) >= a.n_lpages) {
+            report(a.dev_status, QSA_DEV_BAD_CELL);
+            return -1;
+        }
+        const int pp = __ldg(a.page_table + (cell >> 6));
+        if (pp >= a.n_ppages) {
+            report(a.dev_status, QSA_DEV_BAD_PAGE);
+            return -1;
+        }
+        return pp;
+    };
+    auto issue = [&](int cell, int page, int st) {
+        float sc = 0.f;
+        const bool ok = page >= 0;
+        if (ok) {
+            const size_t row = ((size_t)page * a.n_kv + h) * kPage + (cell & (kPage - 1));
+            const int8_t* src = (kv ? a.v_pool : a.k_pool) + row * kHeadDim;
+            const uint32_t dst = smem_u32(&s.raw[st][kv][slot][0]);
+#pragma unroll
+            for (int seg = 0; seg < 8; ++seg) cp_async16(dst + ((seg ^ (slot & 7)) << 4), src + seg * 16);
+            sc = __half2float(__ushort_as_half(__ldg((kv ? a.v_scale : a.k_scale) + row)));
+        }
+        if (kv) s.vs[st][slot] = ok ? sc : 0.f;
+        else s.ks[st][slot] = ok ? sc * kmul : 0.f;
+        const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
+        if (lane == 0) s.valid[st] = vm;
+    };
+
+    int c1 = load_cell(1), c2 = load_cell(2);
+    {
+        const int c0 = load_cell(0);
+        issue(c0, resolve(c0), 0);
+    }
+    cp_async_commit();
+    int p1 = resolve(c1);
+
+    // ---- Q fragments (A operand): rows 0-11 are the KV head's 12 query heads
+    const int g4 = lane >> 2, t4 = lane & 3;
+    const int r0 = g4, r1 = g4 + 8;
+    const bool v1 = r1 < kHeadsPerKv;
+    const uint16_t* q0p = a.q + ((size_t)i * n_heads + h * kHeadsPerKv + r0) * kHeadDim;
+    const uint16_t* q1p = a.q + ((size_t)i * n_heads + h * kHeadsPerKv + (v1 ? r1 : 0)) * kHeadDim;
+    uint32_t qa[8][4];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const int d = kk * 16 + 2 * t4;
+        qa[kk][0] = __ldg(reinterpret_cast<const uint32_t*>(q0p + d));
+        qa[kk][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1p + d)) : 0u;
+        qa[kk][2] = __ldg(reinterpret_cast<const uint32_t*>(q0p + d + 8));
+        qa[kk][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1p + d + 8)) : 0u;
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const uint32_t kb_base = smem_u32(&s.kb[0][0]), vb_base = smem_u32(&s.vb[0][0]);
+
+#pragma unroll 1
+    for (int step = 0; step < n_steps; ++step) {
+        const int st = step & 1;
+        // pipeline: cells of step+3, page of step+2, copies of step+1
+        const int c3 = load_cell(step + 3);
+        const int p2 = resolve(c2);
+        issue(c1, p1, st ^ 1);
+        cp_async_commit();
+        cp_async_wait1();
+        __syncwarp();
+
+        // exact BF16 tiles: lane l converts 64 bytes (half l & 1) of cell (l >> 1) of K and of V
+        {
+            const int cell = lane >> 1, hh = lane & 1;
+#pragma unroll
+            for (int tv = 0; tv < 2; ++tv) {
+                uint8_t* dst = reinterpret_cast<uint8_t*>(tv ? &s.vb[0][0] : &s.kb[0][0]);
+                const uint8_t* src = reinterpret_cast<const uint8_t*>(&s.raw[st][tv][cell][0]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int seg = 4 * hh + k;
+                    const uint4 x = *reinterpret_cast<const uint4*>(src + ((seg ^ (cell & 7)) << 4));
+                    uint4 lo, hi;
+                    int8x16_to_bf16(x, lo, hi);
+                    *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg, 256)) = lo;
+                    *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg + 1, 256)) = hi;
+                }
+            }
+        }
+        __syncwarp();
+
+        // S = Q K^T: 16 rows x 16 cells
+        float sc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+            const int cell = nt * 8 + (lane & 7);
+#pragma unroll
+            for (int kk2 = 0; kk2 < 4; ++kk2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kb_base + swz(cell, 4 * kk2 + (lane >> 3), 256), b0, b1, b2, b3);
+                mma_bf16(sc[nt], qa[2 * kk2], b0, b1);
+                mma_bf16(sc[nt], qa[2 * kk2 + 1], b2, b3);
+            }
+        }
+        // column scale (log2 domain), masked cells -inf
+        const uint32_t vm = s.valid[st];
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c = nt * 8 + 2 * t4;
+            const float2 kc = *reinterpret_cast<const float2*>(&s.ks[st][c]);
+            const bool okA = (vm >> c) & 1u, okB = (vm >> (c + 1)) & 1u;
+            sc[nt][0] = okA ? sc[nt][0] * kc.x : -INFINITY;
+            sc[nt][1] = okB ? sc[nt][1] * kc.y : -INFINITY;
+            sc[nt][2] = okA ? sc[nt][2] * kc.x : -INFINITY;
+            sc[nt][3] = okB ? sc[nt][3] * kc.y : -INFINITY;
+            mx0 = fmax3(mx0, sc[nt][0], sc[nt][1]);
+            mx1 = fmax3(mx1, sc[nt][2], sc[nt][3]);
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        // lazy rescale: the running max only moves when a score exceeds it by 2^32 in p
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const bool need0 = m0 != -INFINITY && mn0 > m0 + kSelRescaleLog2;
+        const bool need1 = m1 != -INFINITY && mn1 > m1 + kSelRescaleLog2;
+        const float al0 = need0 ? fast_exp2(m0 - mn0) : 1.f, al1 = need1 ? fast_exp2(m1 - mn1) : 1.f;
+        if (m0 == -INFINITY || need0) m0 = mn0;
+        if (m1 == -INFINITY || need1) m1 = mn1;
+        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+        if (__any_sync(0xffffffffu, need0 || need1)) {
+#pragma unroll
+            for (int dt = 0; dt < 16; ++dt) {
+                o[dt][0] *= al0;
+                o[dt][1] *= al0;
+                o[dt][2] *= al1;
+                o[dt][3] *= al1;
+            }
+        }
+        float ps0 = 0.f, ps1 = 0.f;
+        uint32_t af[4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c = nt * 8 + 2 * t4;
+            const float2 vc = *reinterpret_cast<const float2*>(&s.vs[st][c]);
+            const float e0 = fast_exp2(sc[nt][0] - mu0), e1 = fast_exp2(sc[nt][1] - mu0);
+            const float e2 = fast_exp2(sc[nt][2] - mu1), e3 = fast_exp2(sc[nt][3] - mu1);
+            ps0 += e0 + e1;
+            ps1 += e2 + e3;
+            af[2 * nt] = pack_bf16x2(e0 * vc.x, e1 * vc.y);       // row r0: A fragment a0 / a2
+            af[2 * nt + 1] = pack_bf16x2(e2 * vc.x, e3 * vc.y);   // row r1: a1 / a3
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+        // O += P V: the 16 cells are one k16 step
+        {
+            const int cell = ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int dn = 0; dn < 16; dn += 2) {
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vb_base + swz(cell, dn + (lane >> 4), 256), b0, b1, b2, b3);
+                mma_bf16(o[dn], af, b0, b1);
+                mma_bf16(o[dn + 1], af, b2, b3);
+            }
+        }
+        __syncwarp();   // the BF16 tiles are rewritten next step
+        c1 = c2;
+        c2 = c3;
+        p1 = p2;
+    }
+    cp_async_wait1();   // nothing left in flight when the warp exits (the last group is empty)
+
+    // ---- O / l for rows 0-11
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+    float* out0 = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + r0) * kHeadDim;
+    float* out1 = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + (v1 ? r1 : 0)) * kHeadDim;
+#pragma unroll
+    for (int dt = 0; dt < 16; ++dt) {
+        const int d = dt * 8 + 2 * t4;
+        *reinterpret_cast<float2*>(out0 + d) = make_float2(o[dt][0] * inv0, o[dt][1] * inv0);
+        if (v1) *reinterpret_cast<float2*>(out1 + d) = make_float2(o[dt][2] * inv1, o[dt][3] * inv1);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_select_attn(const SelArgs& a, cudaStream_t stream) {
+    const int smem = (int)(kSelWarps * sizeof(WarpSmem));
+    cudaError_t e = cudaFuncSetAttribute(select_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const long long items = (long long)a.n_q * a.n_kv;
+    const unsigned grid = (unsigned)((items + kSelWarps - 1) / kSelWarps);
+    select_attn_kernel<<<grid, kSelThreads, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace qsa

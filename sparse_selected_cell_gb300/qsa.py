@@ -56,6 +56,8 @@ def lib():
         L.qsa_prompt_attn_static.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _I, _I,
                                              _P, _P]
         L.qsa_prompt_attn_static.restype = ctypes.c_int
+        L.qsa_select_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
+        L.qsa_select_attn.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -163,6 +165,32 @@ def prompt_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
                                int(workspace.numel() * workspace.element_size()), int(union_stride), int(variant),
                                _ptr(dev_status), _stream(stream))
     _check("qsa_prompt_attn", rc)
+    return out
+
+
+def select_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
+                sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Per-position attention without unions (qsa_select_attn) -> out float32 [n_q, n_kv*12, 128]."""
+    _dev(q, "q", _B16)
+    _dev(k_pool, "k_pool", (torch.int8,))
+    _dev(v_pool, "v_pool", (torch.int8,))
+    _dev(k_scale, "k_scale", _H16)
+    _dev(v_scale, "v_scale", _H16)
+    _dev(page_table, "page_table", (torch.int32,))
+    _dev(sel, "sel", (torch.int32,))
+    _dev(sel_count, "sel_count", (torch.int32,))
+    n_q, n_heads = int(q.shape[0]), int(q.shape[1])
+    n_kv = n_heads // gen.HEADS_PER_KV
+    if out is None:
+        out = torch.empty((n_q, n_heads, gen.HEAD_DIM), dtype=torch.float32, device=q.device)
+    _dev(out, "out", (torch.float32,))
+    if sm_scale is None:
+        sm_scale = gen.HEAD_DIM ** -0.5
+    rc = lib().qsa_select_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
+                               int(page_table.shape[0]), int(k_pool.shape[0]), n_kv, _ptr(sel), _ptr(sel_count),
+                               int(sel.shape[1]), n_q, float(sm_scale), _ptr(out), _ptr(dev_status), _stream(stream))
+    _check("qsa_select_attn", rc)
     return out
 
 
