@@ -11,14 +11,14 @@
 // in windows of kWindow cells held as a byte map in shared memory (byte = the
 // 8-position mask); a context up to kWindow cells is one window.  Each list is
 // sorted, so its cells inside a window form one contiguous index range (found
-// by binary search only when there are several windows).  The 8 ranges are
-// marked as one flattened index space, eight loads in flight per thread before
-// their ORs of bit j into the cell's byte (OR is order-independent, so the
-// result is deterministic).  The window is then compacted in cell order: every
-// thread takes 16 consecutive bytes, counts the non-zero ones, and a block
-// prefix sum (warp shuffles + one shared-memory pass over the warp totals)
-// gives each thread its output offset.  Output is sorted by construction and
-// bit-exact.
+// by binary search only when there are several windows).  Two warps mark each
+// list, eight loads in flight per lane before their ORs of bit j into the
+// cell's byte (OR is order-independent, so the result is deterministic).  The
+// window is then compacted in cell order: each warp counts the non-zero bytes
+// of its contiguous share of the map, one shared-memory pass over the warp
+// totals gives each warp its output offset, and each warp writes its entries
+// with warp-level prefix sums, visiting only the non-zero bytes.  Output is
+// sorted by construction and bit-exact.
 #include "qsa_common.cuh"
 
 namespace qsa {
@@ -36,6 +36,12 @@ __device__ __forceinline__ int lower_bound(const int32_t* __restrict__ a, int n,
         else hi = mid;
     }
     return lo;
+}
+
+// bit b (b = 0..3) set when byte b of w is non-zero
+__device__ __forceinline__ uint32_t nonzero_mask4(uint32_t w) {
+    const uint32_t t = (((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) & 0x80808080u;   // bit 7 of each non-zero byte
+    return (((t >> 7) * 0x00204081u) >> 21) & 0xFu;                             // gather bits 0, 8, 16, 24
 }
 
 __device__ __forceinline__ int nonzero_bytes(uint32_t w) {
@@ -112,77 +118,81 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
             s_end[tid] = e;
         }
         __syncthreads();
-        // 3. mark: bit j of the byte of every cell in list j; the lists' ranges
-        // are one index space, kMarkUnroll loads per thread in flight at once
-        int pre[kGroup + 1];
-        pre[0] = 0;
+        // 3. mark: bit j of the byte of every cell in list j.  Warps w and w + 8
+        // take list w % 8, kMarkUnroll loads per lane in flight before the ORs.
+        {
+            const int j = warp & (kGroup - 1);
+            if (j < nj) {
+                const int32_t* lst = sel + (size_t)(q_begin + j) * sel_stride;
+                const int e = s_end[j];
+                constexpr int kStride = (kThreads / 32 / kGroup) * 32;   // lanes on one list
+                for (int t0 = s_beg[j] + (warp / kGroup) * 32 + lane; t0 < e; t0 += kStride * kMarkUnroll) {
+                    int cell[kMarkUnroll];
 #pragma unroll
-        for (int j = 0; j < kGroup; ++j) pre[j + 1] = pre[j] + (j < nj ? s_end[j] - s_beg[j] : 0);
-        const int total = pre[kGroup];
-        for (int base = 0; base < total; base += kThreads * kMarkUnroll) {
-            int cell[kMarkUnroll], jj[kMarkUnroll];
-#pragma unroll
-            for (int u = 0; u < kMarkUnroll; ++u) {
-                const int idx = base + u * kThreads + tid;
-                int j = 0, start = 0;
-#pragma unroll
-                for (int k = 1; k < kGroup; ++k)
-                    if (idx >= pre[k]) {
-                        j = k;
-                        start = pre[k];
+                    for (int u = 0; u < kMarkUnroll; ++u) {
+                        const int t = t0 + u * kStride;
+                        cell[u] = t < e ? __ldg(lst + t) : INT32_MIN;
                     }
-                jj[u] = idx < total ? j : -1;
-                cell[u] = idx < total
-                              ? __ldg(sel + (size_t)(q_begin + j) * sel_stride + s_beg[j] + (idx - start))
-                              : 0;
-            }
 #pragma unroll
-            for (int u = 0; u < kMarkUnroll; ++u) {
-                const long long off = (long long)cell[u] - w0;
-                if (jj[u] >= 0 && off >= 0 && off < span)
-                    atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + jj[u]));
+                    for (int u = 0; u < kMarkUnroll; ++u) {
+                        const long long off = (long long)cell[u] - w0;
+                        if (cell[u] != INT32_MIN && off >= 0 && off < span)
+                            atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + j));
+                    }
+                }
             }
         }
         __syncthreads();
-        // 4. compact the window in cell order
-        for (int p0 = 0; p0 < n_pieces; p0 += kThreads) {
-            const int p = p0 + tid;
-            uint4 v = p < n_pieces ? smem_map[p] : make_uint4(0, 0, 0, 0);
-            const int n = nonzero_bytes(v.x) + nonzero_bytes(v.y) + nonzero_bytes(v.z) + nonzero_bytes(v.w);
+        // 4. compact the window in cell order.  Warp w owns the contiguous pieces
+        // [w * per_warp, (w + 1) * per_warp): it counts their non-zero bytes, one
+        // block pass turns the warp totals into offsets, and each warp then writes
+        // its pieces' entries with warp-level scans only.
+        const int per_warp = (n_pieces + kThreads / 32 - 1) / (kThreads / 32);
+        const int p_lo = min(n_pieces, warp * per_warp), p_hi = min(n_pieces, p_lo + per_warp);
+        int cnt_w = 0;
+        for (int p = p_lo + lane; p < p_hi; p += 32) {
+            const uint4 v = smem_map[p];
+            cnt_w += nonzero_bytes(v.x) + nonzero_bytes(v.y) + nonzero_bytes(v.z) + nonzero_bytes(v.w);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt_w += __shfl_xor_sync(0xffffffffu, cnt_w, o);
+        if (lane == 0) s_warp[warp] = cnt_w;
+        __syncthreads();
+        int run = written, total = 0;   // run: output index of this warp's first entry
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const int x = s_warp[w];
+            run += w < warp ? x : 0;
+            total += x;
+        }
+        for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
+            const int p = p0 + lane;
+            const uint4 v = p < p_hi ? smem_map[p] : make_uint4(0, 0, 0, 0);
+            uint32_t nzm = nonzero_mask4(v.x) | (nonzero_mask4(v.y) << 4) | (nonzero_mask4(v.z) << 8) |
+                           (nonzero_mask4(v.w) << 12);   // one bit per non-zero byte of the piece
+            const int n = __popc(nzm);
             int incl = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (lane == 31) s_warp[warp] = incl;
-            __syncthreads();
-            int before = 0, total = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) {
-                const int x = s_warp[w];
-                before += w < warp ? x : 0;
-                total += x;
-            }
-            if (n > 0) {
-                int idx = written + before + incl - n;
-                const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-                const long long cell0 = w0 + (long long)p * 16;
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint32_t m = (words[k >> 2] >> ((k & 3) * 8)) & 0xFFu;
-                    if (m) {
-                        if (idx < ustride) {
-                            ucell[out_base + idx] = (int32_t)(cell0 + k);
-                            umask[out_base + idx] = (uint8_t)m;
-                        }
-                        ++idx;
-                    }
+            int idx = run + incl - n;
+            const long long cell0 = w0 + (long long)p * 16;
+            while (nzm) {
+                const int k = __ffs(nzm) - 1;
+                nzm &= nzm - 1;
+                const uint32_t wd = k < 8 ? (k < 4 ? v.x : v.y) : (k < 12 ? v.z : v.w);
+                if (idx < ustride) {
+                    ucell[out_base + idx] = (int32_t)(cell0 + k);
+                    umask[out_base + idx] = (uint8_t)__byte_perm(wd, 0u, (uint32_t)(k & 3));
                 }
+                ++idx;
             }
-            written += total;
-            __syncthreads();      // s_warp is reused by the next piece round
+            run += __shfl_sync(0xffffffffu, incl, 31);
         }
+        written += total;
+        __syncthreads();      // the map and s_warp are reused by the next window
     }
     if (tid == 0) {
         if (written > ustride) {
