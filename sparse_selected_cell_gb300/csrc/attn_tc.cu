@@ -18,9 +18,10 @@
 //              always share one running max.  Per chunk a warp reads its 32 S
 //              columns from TMEM, scales each by its K scale, masks cells its
 //              query did not select (one 64-bit selection word per query),
-//              computes p = 2^(C (s - m)) (C = sm_scale * log2(e); the running
-//              max m only moves when a score exceeds it by more than 2^32 in p,
-//              and O is rescaled in TMEM only then), writes P = p * (V scale)
+//              computes p = 2^(v - m) in the exp2 domain (the table's K scale
+//              carries sm_scale * log2(e); the running max m only moves when a
+//              score exceeds it by more than 2^32 in p, and O is rescaled in
+//              TMEM only then), writes P = p * (V scale)
 //              as BF16 over its own S columns, and keeps its own FP32 sum of p.  At the
 //              end the pair adds their sums and each stores half of O's columns.
 //              They also write the Q rows into the shared-memory Q tile first.
@@ -81,7 +82,7 @@ constexpr uint64_t kWaitNs = 1000000000ull;
 
 struct RawTab {
     int32_t row[kChunk];           // pool row (page * n_kv + h) * 64 + cell % 64; -1 for a masked cell
-    float ks[kChunk];              // K scale; 0 for a masked cell
+    float ks[kChunk];              // K scale * sm_scale * log2(e); 0 for a masked cell
     float vs[kChunk];              // V scale; 0 for a masked cell
     uint64_t rowmask[8];           // bit c: query j of the group selected resident cell c
 };
@@ -266,7 +267,7 @@ __device__ void producer_role(const Ctx& c, int lane) {
         for (int k = 0; k < 2; ++k) {
             const bool ok = r0[k] >= 0;
             T->row[lane + 32 * k] = ok ? r0[k] : -1;
-            T->ks[lane + 32 * k] = ok ? __half2float(__ushort_as_half(s0.ks[k])) : 0.f;
+            T->ks[lane + 32 * k] = ok ? __half2float(__ushort_as_half(s0.ks[k])) * c.kmul : 0.f;
             T->vs[lane + 32 * k] = ok ? __half2float(__ushort_as_half(s0.vs[k])) : 0.f;
         }
 #pragma unroll
@@ -487,16 +488,16 @@ __device__ __forceinline__ void scale_mask16(uint32_t* s, uint32_t sel, bool uni
     }
 }
 
-// Weights e = 2^(C*v - C*m) for 16 columns: e is added to la / lb (the row's
+// Weights e = 2^(v - m) for 16 columns: e is added to la / lb (the row's
 // sum), and e * (V scale) goes out as 8 packed BF16 pairs -- the P that meets
 // the exact BF16 V rows in P V (vs: the 16 columns' V scales in shared memory).
-__device__ __forceinline__ void exp16(const uint32_t* s, const float* vs, float2 C2, float2 nCm, uint32_t* p,
+__device__ __forceinline__ void exp16(const uint32_t* s, const float* vs, float2 nm, uint32_t* p,
                                       float2& la, float2& lb) {
 #pragma unroll
     for (int u4 = 0; u4 < 4; ++u4) {
         const float4 vq = *reinterpret_cast<const float4*>(vs + 4 * u4);
-        const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(s[4 * u4]), __uint_as_float(s[4 * u4 + 1])), C2, nCm);
-        const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(s[4 * u4 + 2]), __uint_as_float(s[4 * u4 + 3])), C2, nCm);
+        const float2 x01 = __fadd2_rn(make_float2(__uint_as_float(s[4 * u4]), __uint_as_float(s[4 * u4 + 1])), nm);
+        const float2 x23 = __fadd2_rn(make_float2(__uint_as_float(s[4 * u4 + 2]), __uint_as_float(s[4 * u4 + 3])), nm);
         const float2 e01 = make_float2(fast_exp2(x01.x), fast_exp2(x01.y));
         const float2 e23 = make_float2(fast_exp2(x23.x), fast_exp2(x23.y));
         la = __fadd2_rn(la, e01);
@@ -530,10 +531,10 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(c, BAR_Q_READY));
     }
-    // Scores are kept in units of q.k * (K scale); the constant sm_scale * log2(e)
-    // is applied inside the exponent: p = 2^(C * (v - m)).
-    const float C = c.kmul;
-    const float thresh = kRescaleLog2 / C;
+    // Scores are kept in log2 units, v = q.k * (K scale) * sm_scale * log2(e), and
+    // masked after all scaling, so p = 2^(v - m) holds for any sm_scale (0 gives
+    // equal weights; no -inf is ever multiplied).
+    const float thresh = kRescaleLog2;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < c.n_chunks; ++t) {
@@ -563,20 +564,20 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         const float m_new = fmax3(m, fmaxf(mx, my), xb[(hf ^ 1) * kRows + r]);
         const bool need = (m != -INFINITY) && (m_new > m + thresh);
         const float m_use = (m == -INFINITY || need) ? m_new : m;
-        const float alpha = need ? fast_exp2(C * (m - m_new)) : 1.f;
+        const float alpha = need ? fast_exp2(m - m_new) : 1.f;
         const float m_sub = m_use == -INFINITY ? 0.f : m_use;
         uint32_t p[16];
-        const float2 C2 = make_float2(C, C), nCm = make_float2(-C * m_sub, -C * m_sub);
+        const float2 nm = make_float2(-m_sub, -m_sub);
         float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
         const float* vsp = &T->vs[32 * hf];
         if (act_lo) {
-            exp16(&sv[0], vsp, C2, nCm, &p[0], la, lb);
+            exp16(&sv[0], vsp, nm, &p[0], la, lb);
         } else {
 #pragma unroll
             for (int v = 0; v < 8; ++v) p[v] = 0u;
         }
         if (act_hi) {
-            exp16(&sv[16], vsp + 16, C2, nCm, &p[8], la, lb);
+            exp16(&sv[16], vsp + 16, nm, &p[8], la, lb);
         } else {
 #pragma unroll
             for (int v = 0; v < 8; ++v) p[8 + v] = 0u;

@@ -197,3 +197,46 @@ def test_chunk_placement_edge_cases(qsa, variant):
     assert st == 0
     ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, sel, cnt, w.n_kv, w.sm_scale)
     check_close(got, ref, "chunk placement edge cases")
+
+
+def _run_scaled(qsa, w, variant, sm_scale, **over):
+    d = qsa.to_device(w)
+    d.update({k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in over.items()})
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = qsa.prompt_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"],
+                          d["sel"], d["sel_count"], sm_scale=sm_scale, variant=variant, dev_status=status)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), int(status.item())
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_zero_scale_is_the_mean_of_v(qsa, variant):
+    """sm_scale = 0 makes every selected, resident cell weigh the same: each row is the
+    plain mean of its cells' dequantised V (a closed form, computed here in numpy)."""
+    w = gen.make(2, n_q=24, nonresident_frac=0.1, seed=41)
+    got, st = _run_scaled(qsa, w, variant, 0.0)
+    assert st == 0
+    v = w.v_pool.astype(np.float64) * w.v_scale.astype(np.float64)[..., None]   # [page][kv][cell][d]
+    ref = np.zeros_like(got, dtype=np.float64)
+    for i in range(w.n_q):
+        cells = w.sel[i, :w.sel_count[i]]
+        pages = w.page_table[cells >> 6]
+        keep = pages >= 0
+        for kh in range(w.n_kv):
+            rows = v[pages[keep], kh, cells[keep] & 63]
+            if len(rows):
+                ref[i, kh * 12:(kh + 1) * 12] = rows.mean(axis=0)
+    check_close(got, ref, "sm_scale = 0")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_negative_scales_and_custom_sm_scale(qsa, variant):
+    """FP16 scales of either sign and a non-default sm_scale, against the oracle."""
+    w = gen.make(2, n_q=40, seed=43)
+    rng = np.random.default_rng(5)
+    ks = (w.k_scale * rng.choice([-1.0, 1.0], size=w.k_scale.shape)).astype(np.float16)
+    vs = (w.v_scale * rng.choice([-1.0, 1.0], size=w.v_scale.shape)).astype(np.float16)
+    got, st = _run_scaled(qsa, w, variant, 0.05, k_scale=ks.view(np.int16), v_scale=vs.view(np.int16))
+    assert st == 0
+    ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, ks, vs, w.page_table, w.sel, w.sel_count, w.n_kv, 0.05)
+    check_close(got, ref, "negative scales")
