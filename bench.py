@@ -65,7 +65,7 @@ def parse():
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--variant", type=int, default=0, help="0 default, 1 tcgen05, 2 mma.sync")
+    p.add_argument("--variant", type=int, default=0, help="0 default, 1 tcgen05, 2 mma.sync, 3 tcgen05 wide")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -429,9 +429,10 @@ def main():
         t_hbm = alg["bytes"] / (hbm * 1e9) * 1e3
         t_tc = alg["flops"] / (bf16_sus * 1e12) * 1e3
         resolved = args.variant or qsa.default_variant()
-        kernel = "attn_tc_kernel" if resolved == qsa.ATTN_TCGEN05 else "attn_mma_kernel"
-        srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in
-                (("attn_tc.cu", "tc_ptx.cuh") if kernel == "attn_tc_kernel" else ("attn_mma.cu",)) + ("qsa_common.cuh",)]
+        kernel, files = {qsa.ATTN_TCGEN05: ("attn_tc_kernel", ("attn_tc.cu", "tc_ptx.cuh")),
+                         qsa.ATTN_MMA_SYNC: ("attn_mma_kernel", ("attn_mma.cu",)),
+                         qsa.ATTN_TCGEN05_WIDE: ("attn_wide_kernel", ("attn_wide.cu", "tc_ptx.cuh"))}[resolved]
+        srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in files + ("qsa_common.cuh",)]
         traffic, digest = read_traffic(kernel, srcs)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -440,7 +441,7 @@ def main():
             "config": {"workload": workload_desc(w), "l2": "inputs larger than L2: %.0f MB read + %.0f MB written per step"
                        % ((sum(v.numel() * v.element_size() for v in d.values())) / 1e6, out.numel() * 4 / 1e6),
                        "mean_union_cells": round(alg["mean_union"], 1), "union_ratio": round(alg["union_ratio"], 3),
-                       "variant": {1: "tcgen05", 2: "mma.sync"}[resolved], "parallelism": f"dp{world}"},
+                       "variant": {1: "tcgen05", 2: "mma.sync", 3: "tcgen05-wide"}[resolved], "parallelism": f"dp{world}"},
             "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "kernel": kernel,
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": traffic, "peak_source": src,

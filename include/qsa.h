@@ -76,11 +76,14 @@ enum {
 /* Attention kernel variants (all sm_103a).  QSA_ATTN_DEFAULT picks the fastest. */
 enum {
     QSA_ATTN_DEFAULT = 0,
-    QSA_ATTN_TCGEN05 = 1,   /* tcgen05.mma with TMEM accumulators, warp-specialised pipeline */
-    QSA_ATTN_MMA_SYNC = 2   /* warp-level mma.sync m16n8k16 (legacy tensor path, for comparison) */
+    QSA_ATTN_TCGEN05 = 1,   /* tcgen05.mma with TMEM accumulators, warp-specialised pipeline,
+                               one CTA per (group, KV head), 64-cell chunks, two CTAs per SM */
+    QSA_ATTN_MMA_SYNC = 2,  /* warp-level mma.sync m16n8k16 (legacy tensor path, for comparison) */
+    QSA_ATTN_TCGEN05_WIDE = 3  /* tcgen05, persistent, one CTA per SM over many (group, KV head)
+                                  items, 128-cell chunks, the Q operand in TMEM */
 };
 
-/* The variant QSA_ATTN_DEFAULT resolves to in this build (QSA_ATTN_TCGEN05 or QSA_ATTN_MMA_SYNC). */
+/* The variant QSA_ATTN_DEFAULT resolves to in this build (one of the values above). */
 int qsa_attn_default_variant(void);
 
 /* Human-readable name of a qsa_status value.  Never NULL. */

@@ -39,7 +39,7 @@ int check_attn_args(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     const uint16_t* v_scale, const int32_t* page_table, int32_t n_lpages, int32_t n_ppages,
                     int32_t n_kv, int32_t n_q, float* out, int32_t variant) {
     if (n_q < 0 || n_lpages < 0 || n_ppages < 0 || n_kv <= 0) return QSA_ERR_ARG;
-    if (variant < QSA_ATTN_DEFAULT || variant > QSA_ATTN_MMA_SYNC) return QSA_ERR_ARG;
+    if (variant < QSA_ATTN_DEFAULT || variant > QSA_ATTN_TCGEN05_WIDE) return QSA_ERR_ARG;
     if (n_q == 0) return QSA_OK;
     if (!q || !out || !page_table) return QSA_ERR_ARG;
     if (n_ppages > 0 && (!k_pool || !v_pool || !k_scale || !v_scale)) return QSA_ERR_ARG;
@@ -103,6 +103,7 @@ int qsa_union_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (variant == QSA_ATTN_DEFAULT) variant = qsa_attn_default_variant();
     if (variant == QSA_ATTN_TCGEN05) return cuda_status(qsa::launch_attn_tc(a, s));
+    if (variant == QSA_ATTN_TCGEN05_WIDE) return cuda_status(qsa::launch_attn_wide(a, s));
     return cuda_status(qsa::launch_attn_mma(a, s));
 }
 

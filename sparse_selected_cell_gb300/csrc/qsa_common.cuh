@@ -125,6 +125,7 @@ struct AttnArgs {
 
 cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_wide(const AttnArgs& a, cudaStream_t stream);
 
 // Per-position attention (no union): each query over its own selection list.
 struct SelArgs {

@@ -65,7 +65,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity, u
 // *abort becomes non-zero or after `limit_ns` of wall time (then it sets *abort
 // itself); returns false in both cases.  The loop lives out of line so that the
 // many wait sites of a kernel stay small in the instruction cache.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -18,7 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libqsa.so")
 
 QSA_OK, QSA_ERR_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CAPACITY, QSA_ERR_CUDA, QSA_ERR_DEVICE_CHECK = range(6)
-ATTN_DEFAULT, ATTN_TCGEN05, ATTN_MMA_SYNC = 0, 1, 2
+ATTN_DEFAULT, ATTN_TCGEN05, ATTN_MMA_SYNC, ATTN_TCGEN05_WIDE = 0, 1, 2, 3
 DEV_BITS = {1: "bad selection count", 2: "union overflow", 4: "bad cell", 8: "bad page-table entry",
             16: "bad union count", 32: "device wait timeout"}
 
