@@ -396,20 +396,24 @@ __device__ void mma_role(const Ctx& c) {
     constexpr uint32_t idS = tc::idesc_bf16(128, kChunk, false, false);    // A = Q tile, B = K tile, K-major
     constexpr uint32_t idO = tc::idesc_bf16(128, kHeadDim, false, true);   // B = V tile, MN-major
     const int n = c.n_chunks;
+    // Operand descriptors are built once; a K step or another buffer only moves the
+    // 14-bit start-address field (address >> 4), which never carries out of it
+    // (shared-memory addresses are below 256 KB).
+    const uint64_t dq0 = tc::smem_desc(c.base_u + kOffQ, 16, 1024, 2);
+    const uint64_t dk0 = tc::smem_desc(c.base_u + kOffKb, 16, 1024, 2);
+    const uint64_t dv0 = tc::smem_desc(c.base_u + kOffVb, 8192, 1024, 2);
     auto issue_s = [&](int t) -> bool {
         const int b = t % kNB;
         if (t == 0 && !wait_addr(c, bar(c, BAR_Q_READY), 0)) return false;
         if (!wait_addr(c, bar(c, BAR_K_FULL + b), (t / kNB) & 1)) return false;
         tc::fence_after_sync();
-        const uint32_t q_u = c.base_u + kOffQ;
-        const uint32_t kt = c.base_u + kOffKb + b * kTileBytes;
+        const uint64_t dk = dk0 + (uint64_t)((b * kTileBytes) >> 4);
         const uint32_t tS = c.tmem + kColS + 64 * (t & 1);
 #pragma unroll
         for (int k = 0; k < kHeadDim / 16; ++k) {
             const uint32_t koff = (k >> 2) * (kTileBytes / 2) + (k & 3) * 32;
             const uint32_t qoff = (k >> 2) * (kQTileBytes / 2) + (k & 3) * 32;
-            tc::mma_ss(tS, tc::smem_desc(q_u + qoff, 16, 1024, 2), tc::smem_desc(kt + koff, 16, 1024, 2), idS,
-                       k > 0 ? 1u : 0u);
+            tc::mma_ss(tS, dq0 + (qoff >> 4), dk + (koff >> 4), idS, k > 0 ? 1u : 0u);
         }
         tc::commit(bar(c, BAR_S_FULL + (t & 1)));
         tc::commit(bar(c, BAR_K_EMPTY + b));
@@ -420,13 +424,12 @@ __device__ void mma_role(const Ctx& c) {
         if (!wait_addr(c, bar(c, BAR_P_READY + (t & 1)), (t >> 1) & 1)) return false;
         if (!wait_addr(c, bar(c, BAR_V_FULL + b), (t / kNB) & 1)) return false;
         tc::fence_after_sync();
-        const uint32_t vt = c.base_u + kOffVb + b * kTileBytes;
+        const uint64_t dv = dv0 + (uint64_t)((b * kTileBytes) >> 4);
         const uint32_t tP = c.tmem + kColS + 64 * (t & 1);
         const uint32_t tO = c.tmem + kColO;
 #pragma unroll
         for (int k = 0; k < kChunk / 16; ++k)   // P of cells 16k..16k+15: columns 8(k&1) + 32(k>>1)
-            tc::mma_ts(tO, tP + 8 * (k & 1) + 32 * (k >> 1), tc::smem_desc(vt + k * 2048, 8192, 1024, 2), idO,
-                       (t > 0 || k > 0) ? 1u : 0u);
+            tc::mma_ts(tO, tP + 8 * (k & 1) + 32 * (k >> 1), dv + ((k * 2048) >> 4), idO, (t > 0 || k > 0) ? 1u : 0u);
         tc::commit(bar(c, BAR_PV_DONE));
         tc::commit(bar(c, BAR_V_EMPTY + b));
         if (t == n - 1) tc::commit(bar(c, BAR_O_DONE));
