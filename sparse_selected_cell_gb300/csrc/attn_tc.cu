@@ -100,9 +100,14 @@ constexpr uint32_t kOffXchg = kOffRawTab + kNS * (uint32_t)sizeof(RawTab);
 constexpr uint32_t kOffBars = (kOffXchg + 3 * 2 * kRows * 4 + 7u) & ~7u;
 // K and V tiles are filled and freed separately (K is free once S is done, V
 // once P V is done)
-enum { BAR_TAB_FULL = 0, BAR_TAB_EMPTY = kNS, BAR_K_FULL = 2 * kNS, BAR_K_EMPTY = BAR_K_FULL + kNB,
-       BAR_V_FULL = BAR_K_EMPTY + kNB, BAR_V_EMPTY = BAR_V_FULL + kNB, BAR_S_FULL = BAR_V_EMPTY + kNB,
-       BAR_P_READY = BAR_S_FULL + 2, BAR_PV_DONE = BAR_P_READY + 2, BAR_O_DONE, BAR_Q_READY, BAR_DRAIN, NUM_BARS };
+// With two K tiles and two S buffers, "K tile b is free" and "S buffer b is full"
+// are one event (S(t) has completed, t % 2 == b): the loaders wait on S_FULL.  And
+// "P(t) V has completed" is V_EMPTY[t % 2], which the softmax also waits on
+// before a rescale of O.  So the MMA thread commits three barriers per chunk.
+static_assert(kNB == 2, "K tile b and S buffer b share the S_FULL barrier");
+enum { BAR_TAB_FULL = 0, BAR_TAB_EMPTY = kNS, BAR_K_FULL = 2 * kNS, BAR_V_FULL = BAR_K_FULL + kNB,
+       BAR_V_EMPTY = BAR_V_FULL + kNB, BAR_S_FULL = BAR_V_EMPTY + kNB, BAR_P_READY = BAR_S_FULL + 2,
+       BAR_O_DONE = BAR_P_READY + 2, BAR_Q_READY, BAR_DRAIN, NUM_BARS };
 constexpr uint32_t kOffMisc = kOffBars + NUM_BARS * 8;      // tmem base, abort flag
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;           // + alignment slack
@@ -353,7 +358,7 @@ __device__ __forceinline__ bool convert_chunk(const Ctx& c, int ct, int i, const
     uint8_t* vb = c.base + kOffVb + b * kTileBytes;
     uint4 vx[kRowsPerThread];
     load_rows(c.a->v_pool, T, ct, vx);
-    if (!wait_addr(c, bar(c, BAR_K_EMPTY + b), par)) return false;
+    if (!wait_addr(c, bar(c, BAR_S_FULL + b), par)) return false;   // S(i-2) has read K tile b
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) store_row(kb, ct, k, kx[k]);
     tc::fence_proxy_async();
@@ -415,8 +420,7 @@ __device__ void mma_role(const Ctx& c) {
             const uint32_t qoff = (k >> 2) * (kQTileBytes / 2) + (k & 3) * 32;
             tc::mma_ss(tS, dq0 + (qoff >> 4), dk + (koff >> 4), idS, k > 0 ? 1u : 0u);
         }
-        tc::commit(bar(c, BAR_S_FULL + (t & 1)));
-        tc::commit(bar(c, BAR_K_EMPTY + b));
+        tc::commit(bar(c, BAR_S_FULL + (t & 1)));   // also: K tile b is free
         return true;
     };
     auto issue_pv = [&](int t) -> bool {
@@ -430,8 +434,7 @@ __device__ void mma_role(const Ctx& c) {
 #pragma unroll
         for (int k = 0; k < kChunk / 16; ++k)   // P of cells 16k..16k+15: columns 8(k&1) + 32(k>>1)
             tc::mma_ts(tO, tP + 8 * (k & 1) + 32 * (k >> 1), dv + ((k * 2048) >> 4), idO, (t > 0 || k > 0) ? 1u : 0u);
-        tc::commit(bar(c, BAR_PV_DONE));
-        tc::commit(bar(c, BAR_V_EMPTY + b));
+        tc::commit(bar(c, BAR_V_EMPTY + b));   // also: P(t) V has completed
         if (t == n - 1) tc::commit(bar(c, BAR_O_DONE));
         return true;
     };
@@ -591,7 +594,7 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         if (__any_sync(0xffffffffu, need)) {
             // O must hold every earlier P V before it is rescaled: wait for PV(t-1);
             // this warp rescales its half of O's columns
-            if (!(ok = wait_addr(c, bar(c, BAR_PV_DONE), (t - 1) & 1))) break;
+            if (!(ok = wait_addr(c, bar(c, BAR_V_EMPTY + (t - 1) % kNB), ((t - 1) / kNB) & 1))) break;
             tc::fence_after_sync();
 #pragma unroll 1
             for (int q8 = 0; q8 < 4; ++q8) {
@@ -674,7 +677,6 @@ __global__ void __launch_bounds__(kThreadsTc, kCtasPerSm) attn_tc_kernel(const _
         }
         for (int b = 0; b < kNB; ++b) {
             tc::mbar_init(bar(c, BAR_K_FULL + b), kConvWarps);
-            tc::mbar_init(bar(c, BAR_K_EMPTY + b), 1);
             tc::mbar_init(bar(c, BAR_V_FULL + b), kConvWarps);
             tc::mbar_init(bar(c, BAR_V_EMPTY + b), 1);
         }
@@ -682,7 +684,6 @@ __global__ void __launch_bounds__(kThreadsTc, kCtasPerSm) attn_tc_kernel(const _
             tc::mbar_init(bar(c, BAR_S_FULL + sb), 1);
             tc::mbar_init(bar(c, BAR_P_READY + sb), kSoftWarps);
         }
-        tc::mbar_init(bar(c, BAR_PV_DONE), 1);
         tc::mbar_init(bar(c, BAR_O_DONE), 1);
         tc::mbar_init(bar(c, BAR_Q_READY), kSoftWarps + 1);   // softmax warps + the producer (pad rows)
         tc::mbar_init(bar(c, BAR_DRAIN), 1);
