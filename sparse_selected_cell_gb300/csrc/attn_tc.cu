@@ -332,16 +332,26 @@ __device__ __forceinline__ bool prefetch_k(const Ctx& c, int ct, int i, uint4 (&
     return true;
 }
 
-// Converts the thread's 2 x 8 bytes of row k and stores them as BF16 into both
-// halves of the 128-byte-swizzled tile at `tile`.
+// Converts the thread's 2 x 8 bytes of row k and stores them into both halves of
+// the 128-byte-swizzled tile at `tile`: as FP16 for K (the operand of S, whose
+// other operand Q is FP16 too; 3 integer/logic instructions per 4 values) and as
+// BF16 for V (whose partner P needs BF16's exponent range; 6 per 4 values).
+template <bool kF16>
 __device__ __forceinline__ void store_row(uint8_t* tile, int ct, int k, uint4 x) {
     const int i = ct & 7, row = (ct >> 3) + (kConvThreads / 8) * k;
     const uint32_t off = (uint32_t)row * 128 + ((uint32_t)(i ^ (row & 7)) << 4);
     uint4 lo, hi;
-    int8x4_to_bf16(x.x, lo.x, lo.y);
-    int8x4_to_bf16(x.y, lo.z, lo.w);
-    int8x4_to_bf16(x.z, hi.x, hi.y);
-    int8x4_to_bf16(x.w, hi.z, hi.w);
+    if (kF16) {
+        int8x4_to_f16(x.x, lo.x, lo.y);
+        int8x4_to_f16(x.y, lo.z, lo.w);
+        int8x4_to_f16(x.z, hi.x, hi.y);
+        int8x4_to_f16(x.w, hi.z, hi.w);
+    } else {
+        int8x4_to_bf16(x.x, lo.x, lo.y);
+        int8x4_to_bf16(x.y, lo.z, lo.w);
+        int8x4_to_bf16(x.z, hi.x, hi.y);
+        int8x4_to_bf16(x.w, hi.z, hi.w);
+    }
     *reinterpret_cast<uint4*>(tile + off) = lo;
     *reinterpret_cast<uint4*>(tile + kTileBytes / 2 + off) = hi;
 }
@@ -360,14 +370,14 @@ __device__ __forceinline__ bool convert_chunk(const Ctx& c, int ct, int i, const
     load_rows(c.a->v_pool, T, ct, vx);
     if (!wait_addr(c, bar(c, BAR_S_FULL + b), par)) return false;   // S(i-2) has read K tile b
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) store_row(kb, ct, k, kx[k]);
+    for (int k = 0; k < kRowsPerThread; ++k) store_row<true>(kb, ct, k, kx[k]);
     tc::fence_proxy_async();
     __syncwarp();
     if ((ct & 31) == 0) tc::mbar_arrive(bar(c, BAR_K_FULL + b));
     if (!prefetch_k(c, ct, i + 1, kn)) return false;
     if (!wait_addr(c, bar(c, BAR_V_EMPTY + b), par)) return false;
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) store_row(vb, ct, k, vx[k]);
+    for (int k = 0; k < kRowsPerThread; ++k) store_row<false>(vb, ct, k, vx[k]);
     tc::fence_proxy_async();
     __syncwarp();
     if ((ct & 31) == 0) {
@@ -398,7 +408,8 @@ __device__ void converter_role(const Ctx& c, int ct) {
 // order, so P(t-2) is read before S(t) overwrites it); that makes the order
 // above the only one possible.  P(t) V needs P(t) and chunk t's V tile.
 __device__ void mma_role(const Ctx& c) {
-    constexpr uint32_t idS = tc::idesc_bf16(128, kChunk, false, false);    // A = Q tile, B = K tile, K-major
+    // A = Q tile, B = K tile, both FP16 (format fields, bits 7-12, zero), K-major
+    constexpr uint32_t idS = tc::idesc_bf16(128, kChunk, false, false) & ~((7u << 7) | (7u << 10));
     constexpr uint32_t idO = tc::idesc_bf16(128, kHeadDim, false, true);   // B = V tile, MN-major
     const int n = c.n_chunks;
     // Operand descriptors are built once; a K step or another buffer only moves the
@@ -525,13 +536,46 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const size_t row_off = ((size_t)(c.q_begin + j) * c.n_heads + (size_t)c.h * kHeadsPerKv + hq) * kHeadDim;
     float* xchg = reinterpret_cast<float*>(c.base + kOffXchg);   // [parity][half][row]; slots 2: row sums
-    {   // Q row r, this warp's 64-column half -> the swizzled K-major Q tile
+    // Q row r, this warp's 64-element half -> FP16 in the swizzled K-major Q tile.
+    // BF16 -> FP16 is exact for |q| in [2^-17, 2^16); a row whose largest |q| is
+    // 2^14 or more, or below 2^-10, is stored times 2^-e (e puts that largest value
+    // in [2^12, 2^13)), and its scores are multiplied back by 2^e, both exact.
+    float rs = 1.f;
+    bool qscaled = false;
+    {
+        uint4 x[8];
+        float amax = 0.f;
+#pragma unroll
+        for (int q16 = 0; q16 < 8; ++q16) {
+            x[q16] = row_ok ? __ldg(reinterpret_cast<const uint4*>(a.q + row_off) + 8 * hf + q16) : make_uint4(0, 0, 0, 0);
+            amax = fmax3(amax, fmax3(fabsf(bf16_lo(x[q16].x)), fabsf(bf16_hi(x[q16].x)), fabsf(bf16_lo(x[q16].y))),
+                         fmax3(fabsf(bf16_hi(x[q16].y)), fabsf(bf16_lo(x[q16].z)), fabsf(bf16_hi(x[q16].z))));
+            amax = fmax3(amax, fabsf(bf16_lo(x[q16].w)), fabsf(bf16_hi(x[q16].w)));
+        }
+        // the row's largest |q| over both halves (row-sum slots: not used again before the end)
+        float* xl = xchg + 4 * kRows;
+        xl[hf * kRows + r] = amax;
+        pair_sync(quad);
+        amax = fmaxf(amax, xl[(hf ^ 1) * kRows + r]);
+        pair_sync(quad);   // both have read before either writes a row sum there
+        const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;   // floor(log2 amax)
+        // |e| <= 114, so 2^e and 2^-e are normal floats
+        const int e = (amax > 0.f && (ex >= 14 || ex < -10)) ? min(max(ex - 12, -114), 114) : 0;
+        qscaled = __any_sync(0xffffffffu, e != 0);
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e
+        rs = __uint_as_float((uint32_t)(127 + e) << 23);                  // 2^e
         uint8_t* qt = c.base + kOffQ + hf * (kQTileBytes / 2);
 #pragma unroll
         for (int q16 = 0; q16 < 8; ++q16) {
-            uint4 x = make_uint4(0, 0, 0, 0);
-            if (row_ok) x = __ldg(reinterpret_cast<const uint4*>(a.q + row_off) + 8 * hf + q16);
-            *reinterpret_cast<uint4*>(qt + r * 128 + ((q16 ^ (r & 7)) << 4)) = x;
+            uint4 h;
+            uint32_t* hw = reinterpret_cast<uint32_t*>(&h);
+            const uint32_t* bw = reinterpret_cast<const uint32_t*>(&x[q16]);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const __half2 f = __floats2half2_rn(bf16_lo(bw[v]) * down, bf16_hi(bw[v]) * down);
+                hw[v] = *reinterpret_cast<const uint32_t*>(&f);
+            }
+            *reinterpret_cast<uint4*>(qt + r * 128 + ((q16 ^ (r & 7)) << 4)) = h;
         }
         tc::fence_proxy_async();
         __syncwarp();
@@ -560,6 +604,10 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         const bool uni_hi = __all_sync(0xffffffffu, sel_hi == 0 || sel_hi == 0xFFFFu);
         const float* ksp = &T->ks[32 * hf];
         tc::tmem_wait_ld();
+        if (qscaled) {   // rows stored times 2^-e: restore their scores
+#pragma unroll
+            for (int v = 0; v < 32; ++v) sv[v] = __float_as_uint(__uint_as_float(sv[v]) * rs);
+        }
         float mx = -INFINITY, my = -INFINITY;    // two chains for more ILP
         if (act_lo) scale_mask16(&sv[0], sel_lo, uni_lo, ksp, mx, my);
         if (act_hi) scale_mask16(&sv[16], sel_hi, uni_hi, ksp + 16, mx, my);

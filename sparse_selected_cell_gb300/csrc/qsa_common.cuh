@@ -68,6 +68,21 @@ __device__ __forceinline__ void int8x4_to_bf16(uint32_t w, uint32_t& out01, uint
     out23 = bf16x2_sub(l23 & 0xFF7FFF7Fu, l23 & 0xFF80FF80u);
 }
 
+// Exact int8 -> fp16 (fp16's 11-bit significand holds any integer below 2048):
+// the byte biased by 128 (b ^ 0x80 = x + 128, 0..255) becomes the low mantissa
+// byte of fp16 1024 (0x6400), giving 1152 + x; subtracting 1152 (0x6480) leaves x.
+__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ void int8x4_to_f16(uint32_t w, uint32_t& out01, uint32_t& out23) {
+    const uint32_t u = w ^ 0x80808080u;
+    out01 = f16x2_sub(__byte_perm(u, 0x6464u, 0x5140), 0x64806480u);   // [u0, 0x64, u1, 0x64]
+    out23 = f16x2_sub(__byte_perm(u, 0x6464u, 0x5342), 0x64806480u);   // [u2, 0x64, u3, 0x64]
+}
+
 __device__ __forceinline__ void int8x16_to_bf16(uint4 raw, uint4& lo, uint4& hi) {
     int8x4_to_bf16(raw.x, lo.x, lo.y);
     int8x4_to_bf16(raw.y, lo.z, lo.w);

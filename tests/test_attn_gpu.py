@@ -240,3 +240,19 @@ def test_negative_scales_and_custom_sm_scale(qsa, variant):
     assert st == 0
     ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, ks, vs, w.page_table, w.sel, w.sel_count, w.n_kv, 0.05)
     check_close(got, ref, "negative scales")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shift", [20, -20])
+def test_query_magnitudes_far_from_one(qsa, variant, shift):
+    """Q times 2^shift with sm_scale times 2^-shift: the same scores.  Rows whose
+    largest |q| is 2^14 or more, or below 2^-10, take the exact power-of-two row
+    scaling of the FP16 score path; the oracle sees the same scaled inputs."""
+    w = gen.make(2, n_q=40, seed=47)
+    qf = (w.q.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** shift)   # exact
+    q = (qf.view(np.uint32) >> 16).astype(np.uint16)
+    sm = float(2.0 ** -shift / np.sqrt(128.0))
+    got, st = _run_scaled(qsa, w, variant, sm, q=q)
+    assert st == 0
+    ref = oracle.attn_ref(q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, w.sel, w.sel_count, w.n_kv, sm)
+    check_close(got, ref, f"Q x 2^{shift}")
