@@ -297,30 +297,30 @@ __device__ void producer_role(const Ctx& c, int lane) {
 
 // ------------------------------------------------------------------ loaders / converters
 
-// Thread ct of the loader group owns rows (ct >> 3) + 16k, k = 0..3.  Lane i =
-// ct & 7 of each 8-lane group takes bytes [8i, 8i+8) and [64+8i, 64+8i+8) of a
-// row: BF16 columns 8i..8i+7 of the tile's first and of its second 64-column
-// half.  So each 16-byte store of the group fills exactly one 128-byte row of
-// one half (one shared-memory wavefront, conflict-free under the swizzle).
+// Thread ct of the loader group handles, in each of its rows row0(ct) + 16k
+// (k = 0..3), the 16 bytes [16i, 16i+16) with i = col16(ct): one 16-byte load
+// per row, converted to 16 BF16 / FP16 values = two 16-byte stores into half
+// i >> 2 of the tile.  A 16-byte shared store is served 8 lanes at a time; the 8
+// lanes of each such phase take an even and an odd row and opposite halves, so
+// the even row fills the even 16-byte slots of its swizzled 128-byte row and the
+// odd row the odd ones: every phase is one conflict-free wavefront.
 constexpr int kRowsPerThread = kChunk * 8 / kConvThreads;
-__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
-    uint2 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+__device__ __forceinline__ int row0(int ct) { return 4 * (ct >> 5) + 2 * ((ct >> 4) & 1) + ((ct >> 2) & 1); }
+__device__ __forceinline__ int col16(int ct) { return 4 * (((ct >> 3) & 1) ^ ((ct >> 2) & 1)) + (ct & 3); }
+
+__device__ __forceinline__ uint4 ldg_stream16(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ void load_rows(const int8_t* pool, const RawTab* T, int ct, uint4 (&x)[kRowsPerThread]) {
-    const int i = ct & 7;
+    const int i = col16(ct);
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
-        const int r = T->row[(ct >> 3) + (kConvThreads / 8) * k];
-        if (r >= 0) {
-            const int8_t* src = pool + (size_t)r * kHeadDim + 8 * i;
-            const uint2 a = ldg_stream8(src), b = ldg_stream8(src + 64);
-            x[k] = make_uint4(a.x, a.y, b.x, b.y);
-        } else {
-            x[k] = make_uint4(0, 0, 0, 0);
-        }
+        const int r = T->row[row0(ct) + (kConvThreads / 8) * k];
+        x[k] = r >= 0 ? ldg_stream16(pool + (size_t)r * kHeadDim + 16 * i) : make_uint4(0, 0, 0, 0);
     }
 }
 
@@ -332,14 +332,15 @@ __device__ __forceinline__ bool prefetch_k(const Ctx& c, int ct, int i, uint4 (&
     return true;
 }
 
-// Converts the thread's 2 x 8 bytes of row k and stores them into both halves of
-// the 128-byte-swizzled tile at `tile`: as FP16 for K (the operand of S, whose
-// other operand Q is FP16 too; 3 integer/logic instructions per 4 values) and as
-// BF16 for V (whose partner P needs BF16's exponent range; 6 per 4 values).
+// Converts the thread's 16 bytes of row k and stores them into the
+// 128-byte-swizzled tile at `tile`: as FP16 for K (the operand of S, whose other
+// operand Q is FP16 too; 3 integer/logic instructions per 4 values) and as BF16
+// for V (whose partner P needs BF16's exponent range; 6 per 4 values).
 template <bool kF16>
 __device__ __forceinline__ void store_row(uint8_t* tile, int ct, int k, uint4 x) {
-    const int i = ct & 7, row = (ct >> 3) + (kConvThreads / 8) * k;
-    const uint32_t off = (uint32_t)row * 128 + ((uint32_t)(i ^ (row & 7)) << 4);
+    const int i = col16(ct), row = row0(ct) + (kConvThreads / 8) * k;
+    uint8_t* rowp = tile + (i >> 2) * (kTileBytes / 2) + row * 128;
+    const uint32_t c0 = 2u * (uint32_t)(i & 3);
     uint4 lo, hi;
     if (kF16) {
         int8x4_to_f16(x.x, lo.x, lo.y);
@@ -352,8 +353,8 @@ __device__ __forceinline__ void store_row(uint8_t* tile, int ct, int k, uint4 x)
         int8x4_to_bf16(x.z, hi.x, hi.y);
         int8x4_to_bf16(x.w, hi.z, hi.w);
     }
-    *reinterpret_cast<uint4*>(tile + off) = lo;
-    *reinterpret_cast<uint4*>(tile + kTileBytes / 2 + off) = hi;
+    *reinterpret_cast<uint4*>(rowp + ((c0 ^ (row & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(rowp + (((c0 + 1) ^ (row & 7)) << 4)) = hi;
 }
 
 // Chunk i: its K rows are in registers.  Issue its V loads, convert K into the
