@@ -315,20 +315,25 @@ __device__ __forceinline__ uint4 ldg_stream16(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ void load_rows(const int8_t* pool, const RawTab* T, int ct, uint4 (&x)[kRowsPerThread]) {
+// Gathers the thread's 16 bytes of its rows (pool rows `rows`, -1 = masked).
+__device__ __forceinline__ void load_rows(const int8_t* pool, const int (&rows)[kRowsPerThread], int ct,
+                                          uint4 (&x)[kRowsPerThread]) {
     const int i = col16(ct);
 #pragma unroll
-    for (int k = 0; k < kRowsPerThread; ++k) {
-        const int r = T->row[row0(ct) + (kConvThreads / 8) * k];
-        x[k] = r >= 0 ? ldg_stream16(pool + (size_t)r * kHeadDim + 16 * i) : make_uint4(0, 0, 0, 0);
-    }
+    for (int k = 0; k < kRowsPerThread; ++k)
+        x[k] = rows[k] >= 0 ? ldg_stream16(pool + (size_t)rows[k] * kHeadDim + 16 * i) : make_uint4(0, 0, 0, 0);
 }
 
-// Wait for chunk i's table and issue its K row loads (nothing past the last chunk).
-__device__ __forceinline__ bool prefetch_k(const Ctx& c, int ct, int i, uint4 (&kx)[kRowsPerThread]) {
+// Wait for chunk i's table, read the thread's pool rows (kept for the V gather)
+// and issue its K row loads (nothing past the last chunk).
+__device__ __forceinline__ bool prefetch_k(const Ctx& c, int ct, int i, int (&rows)[kRowsPerThread],
+                                           uint4 (&kx)[kRowsPerThread]) {
     if (i >= c.n_chunks) return true;
     if (!wait_addr(c, bar(c, BAR_TAB_FULL + i % kNS), (i / kNS) & 1)) return false;
-    load_rows(c.a->k_pool, raw_tab(c, i % kNS), ct, kx);
+    const RawTab* T = raw_tab(c, i % kNS);
+#pragma unroll
+    for (int k = 0; k < kRowsPerThread; ++k) rows[k] = T->row[row0(ct) + (kConvThreads / 8) * k];
+    load_rows(c.a->k_pool, rows, ct, kx);
     return true;
 }
 
@@ -360,22 +365,22 @@ __device__ __forceinline__ void store_row(uint8_t* tile, int ct, int k, uint4 x)
 // Chunk i: its K rows are in registers.  Issue its V loads, convert K into the
 // K tile of buffer i % kNB, issue chunk i+1's K loads, then convert V.  The V
 // tile is refilled only after P(i-2) V, the K tile after S(i-2).
-__device__ __forceinline__ bool convert_chunk(const Ctx& c, int ct, int i, const uint4 (&kx)[kRowsPerThread],
+__device__ __forceinline__ bool convert_chunk(const Ctx& c, int ct, int i, const int (&rows)[kRowsPerThread],
+                                              const uint4 (&kx)[kRowsPerThread], int (&rn)[kRowsPerThread],
                                               uint4 (&kn)[kRowsPerThread]) {
     const int ts = i % kNS, b = i % kNB;
     const uint32_t par = ((i / kNB) & 1) ^ 1;
-    const RawTab* T = raw_tab(c, ts);
     uint8_t* kb = c.base + kOffKb + b * kTileBytes;
     uint8_t* vb = c.base + kOffVb + b * kTileBytes;
     uint4 vx[kRowsPerThread];
-    load_rows(c.a->v_pool, T, ct, vx);
+    load_rows(c.a->v_pool, rows, ct, vx);
     if (!wait_addr(c, bar(c, BAR_S_FULL + b), par)) return false;   // S(i-2) has read K tile b
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) store_row<true>(kb, ct, k, kx[k]);
     tc::fence_proxy_async();
     __syncwarp();
     if ((ct & 31) == 0) tc::mbar_arrive(bar(c, BAR_K_FULL + b));
-    if (!prefetch_k(c, ct, i + 1, kn)) return false;
+    if (!prefetch_k(c, ct, i + 1, rn, kn)) return false;
     if (!wait_addr(c, bar(c, BAR_V_EMPTY + b), par)) return false;
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) store_row<false>(vb, ct, k, vx[k]);
@@ -393,12 +398,16 @@ __device__ __forceinline__ bool convert_chunk(const Ctx& c, int ct, int i, const
 __device__ void converter_role(const Ctx& c, int ct) {
     if (c.n_chunks == 0) return;
     uint4 kx[kRowsPerThread], kn[kRowsPerThread];
-    if (!prefetch_k(c, ct, 0, kx)) return;
+    int rows[kRowsPerThread], rn[kRowsPerThread];
+    if (!prefetch_k(c, ct, 0, rows, kx)) return;
 #pragma unroll 1
     for (int i = 0; i < c.n_chunks; ++i) {
-        if (!convert_chunk(c, ct, i, kx, kn)) break;
+        if (!convert_chunk(c, ct, i, rows, kx, rn, kn)) break;
 #pragma unroll
-        for (int k = 0; k < kRowsPerThread; ++k) kx[k] = kn[k];
+        for (int k = 0; k < kRowsPerThread; ++k) {
+            kx[k] = kn[k];
+            rows[k] = rn[k];
+        }
     }
 }
 
