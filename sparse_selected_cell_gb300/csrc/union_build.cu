@@ -14,11 +14,13 @@
 // by binary search only when there are several windows).  Two warps mark each
 // list, eight loads in flight per lane before their ORs of bit j into the
 // cell's byte (OR is order-independent, so the result is deterministic).  The
-// window is then compacted in cell order: each warp counts the non-zero bytes
-// of its contiguous share of the map, one shared-memory pass over the warp
-// totals gives each warp its output offset, and each warp writes its entries
-// with warp-level prefix sums, visiting only the non-zero bytes.  Output is
-// sorted by construction and bit-exact.
+// window is then compacted in cell order, visiting only the 64-cell pages that
+// hold a marked cell (a page flag is set while marking; the flagged pages are
+// listed in order by one block scan): each warp counts the entries of its
+// contiguous run of listed pages, one shared-memory pass over the warp totals
+// gives each warp its output offset, and each warp writes its pages' entries
+// with warp-level prefix sums, two cells per lane.  Output is sorted by
+// construction and bit-exact.
 #include "qsa_common.cuh"
 
 namespace qsa {
@@ -38,18 +40,7 @@ __device__ __forceinline__ int lower_bound(const int32_t* __restrict__ a, int n,
     return lo;
 }
 
-// bit b (b = 0..3) set when byte b of w is non-zero
-__device__ __forceinline__ uint32_t nonzero_mask4(uint32_t w) {
-    const uint32_t t = (((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) & 0x80808080u;   // bit 7 of each non-zero byte
-    return (((t >> 7) * 0x00204081u) >> 21) & 0xFu;                             // gather bits 0, 8, 16, 24
-}
-
-__device__ __forceinline__ int nonzero_bytes(uint32_t w) {
-    // bytes of w that are non-zero -> one bit each (bit 7 of each byte), counted
-    uint32_t t = (w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu;
-    t = (t | w) & 0x80808080u;
-    return __popc(t);
-}
+constexpr int kPages = kWindow / kPage;        // 64-cell pages of a window
 
 __global__ void __launch_bounds__(kThreads)
 union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ sel_count, int n_q,
@@ -57,6 +48,9 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
                    int32_t* __restrict__ ucount, int ustride, int32_t* dev_status) {
     extern __shared__ uint4 smem_map[];                  // kWindow bytes
     uint32_t* map32 = reinterpret_cast<uint32_t*>(smem_map);
+    const uint16_t* map16 = reinterpret_cast<const uint16_t*>(smem_map);
+    __shared__ uint8_t s_touched[kPages];                // page p of the window holds a marked cell
+    __shared__ uint16_t s_pages[kPages];                 // the touched pages, in increasing order
     __shared__ int s_cnt[kGroup];
     __shared__ int s_first[kGroup], s_last[kGroup];
     __shared__ int s_beg[kGroup], s_end[kGroup];
@@ -96,11 +90,13 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
         }
     }
     int written = 0;   // union entries produced so far (same value in every thread)
-    for (long long w0 = lo & ~15LL; w0 <= hi; w0 += kWindow) {
-        // 1. clear the byte map of this window (only the part the window can use)
+    for (long long w0 = lo & ~(long long)(kPage - 1); w0 <= hi; w0 += kWindow) {
+        // 1. clear the byte map and the page flags of this window (the part it can use)
         const long long span = min((long long)kWindow, hi - w0 + 1);
-        const int n_pieces = (int)((span + 15) >> 4);
+        const int n_pg = (int)((span + kPage - 1) / kPage);   // pages the compaction may read
+        const int n_pieces = n_pg * (kPage / 16);
         for (int p = tid; p < n_pieces; p += kThreads) smem_map[p] = make_uint4(0, 0, 0, 0);
+        for (int p = tid; p < n_pg; p += kThreads) s_touched[p] = 0;
         // 2. index range of each list inside [w0, w0 + kWindow)
         const bool one_window = hi - w0 < kWindow;
         if (tid < kGroup) {
@@ -118,8 +114,10 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
             s_end[tid] = e;
         }
         __syncthreads();
-        // 3. mark: bit j of the byte of every cell in list j.  Warps w and w + 8
-        // take list w % 8, kMarkUnroll loads per lane in flight before the ORs.
+        // 3. mark: bit j of the byte of every cell in list j, and the cell's page
+        // flag.  Warps w and w + 8 take list w % 8, kMarkUnroll loads per lane in
+        // flight before the ORs.  Cells outside the window (several windows) or
+        // outside [0, n) cannot occur in one window: lo and hi bound every list.
         {
             const int j = warp & (kGroup - 1);
             if (j < nj) {
@@ -136,26 +134,57 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
 #pragma unroll
                     for (int u = 0; u < kMarkUnroll; ++u) {
                         const long long off = (long long)cell[u] - w0;
-                        if (cell[u] != INT32_MIN && off >= 0 && off < span)
+                        if (cell[u] != INT32_MIN && off >= 0 && off < span) {
                             atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + j));
+                            s_touched[off >> 6] = 1;
+                        }
                     }
                 }
             }
         }
         __syncthreads();
-        // 4. compact the window in cell order.  Warp w owns the contiguous pieces
-        // [w * per_warp, (w + 1) * per_warp): it counts their non-zero bytes, one
-        // block pass turns the warp totals into offsets, and each warp then writes
-        // its pieces' entries with warp-level scans only.
-        const int per_warp = (n_pieces + kThreads / 32 - 1) / (kThreads / 32);
-        const int p_lo = min(n_pieces, warp * per_warp), p_hi = min(n_pieces, p_lo + per_warp);
-        int cnt_w = 0;
-        for (int p = p_lo + lane; p < p_hi; p += 32) {
-            const uint4 v = smem_map[p];
-            cnt_w += nonzero_bytes(v.x) + nonzero_bytes(v.y) + nonzero_bytes(v.z) + nonzero_bytes(v.w);
-        }
+        // 4. the touched pages in increasing order: thread t owns flags [2t, 2t+2)
+        {
+            int f[2], c = 0;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt_w += __shfl_xor_sync(0xffffffffu, cnt_w, o);
+            for (int k = 0; k < 2; ++k) {
+                const int p = 2 * tid + k;
+                f[k] = p < n_pg ? s_touched[p] : 0;
+                c += f[k];
+            }
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) s_warp[warp] = incl;
+            __syncthreads();
+            int base = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w) base += w < warp ? s_warp[w] : 0;
+            int idx = base + incl - c;
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (f[k]) s_pages[idx++] = (uint16_t)(2 * tid + k);
+        }
+        int n_touched = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) n_touched += s_warp[w];
+        __syncthreads();
+        // 5. compact the touched pages in cell order.  Warp w owns the contiguous
+        // run of touched pages [w * per_warp, (w + 1) * per_warp); a page is one
+        // step of the warp, lane i holding cells 2i and 2i+1.  The warps' entry
+        // counts go through one block pass, then each warp writes its pages with
+        // warp-level scans.
+        const int per_warp = (n_touched + kThreads / 32 - 1) / (kThreads / 32);
+        const int t_lo = min(n_touched, warp * per_warp), t_hi = min(n_touched, t_lo + per_warp);
+        int cnt_w = 0;
+        for (int t = t_lo; t < t_hi; ++t) {
+            const uint32_t two = map16[s_pages[t] * (kPage / 2) + lane];
+            cnt_w += __popc(__ballot_sync(0xffffffffu, (two & 0xFFu) != 0)) +
+                     __popc(__ballot_sync(0xffffffffu, (two >> 8) != 0));
+        }
         if (lane == 0) s_warp[warp] = cnt_w;
         __syncthreads();
         int run = written, total = 0;   // run: output index of this warp's first entry
@@ -165,12 +194,11 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
             run += w < warp ? x : 0;
             total += x;
         }
-        for (int p0 = p_lo; p0 < p_hi; p0 += 32) {
-            const int p = p0 + lane;
-            const uint4 v = p < p_hi ? smem_map[p] : make_uint4(0, 0, 0, 0);
-            uint32_t nzm = nonzero_mask4(v.x) | (nonzero_mask4(v.y) << 4) | (nonzero_mask4(v.z) << 8) |
-                           (nonzero_mask4(v.w) << 12);   // one bit per non-zero byte of the piece
-            const int n = __popc(nzm);
+        for (int t = t_lo; t < t_hi; ++t) {
+            const int pg = s_pages[t];
+            const uint32_t two = map16[pg * (kPage / 2) + lane];
+            const uint32_t m0 = two & 0xFFu, m1 = two >> 8;
+            const int n = (m0 != 0) + (m1 != 0);
             int incl = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -178,21 +206,22 @@ union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ 
                 if (lane >= o) incl += y;
             }
             int idx = run + incl - n;
-            const long long cell0 = w0 + (long long)p * 16;
-            while (nzm) {
-                const int k = __ffs(nzm) - 1;
-                nzm &= nzm - 1;
-                const uint32_t wd = k < 8 ? (k < 4 ? v.x : v.y) : (k < 12 ? v.z : v.w);
+            const int cell0 = (int)(w0 + (long long)pg * kPage) + 2 * lane;
+            if (m0) {
                 if (idx < ustride) {
-                    ucell[out_base + idx] = (int32_t)(cell0 + k);
-                    umask[out_base + idx] = (uint8_t)__byte_perm(wd, 0u, (uint32_t)(k & 3));
+                    ucell[out_base + idx] = cell0;
+                    umask[out_base + idx] = (uint8_t)m0;
                 }
                 ++idx;
+            }
+            if (m1 && idx < ustride) {
+                ucell[out_base + idx] = cell0 + 1;
+                umask[out_base + idx] = (uint8_t)m1;
             }
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
         written += total;
-        __syncthreads();      // the map and s_warp are reused by the next window
+        __syncthreads();      // the map, the page list and s_warp are reused by the next window
     }
     if (tid == 0) {
         if (written > ustride) {
