@@ -94,3 +94,20 @@ def test_union_rerun_bitwise(qsa, workload):
     b = _gpu_union(qsa, w.sel, w.sel_count)
     for x, y in zip(a[:3], b[:3]):
         assert np.array_equal(x, y)
+
+
+def test_union_whole_pages_across_window_edges(qsa):
+    """Dense runs of whole 64-cell pages, one crossing the 65,536-cell window edge,
+    and a partly filled last page: the compaction walks only the pages that hold a
+    marked cell, so every page boundary and window boundary must come out exact."""
+    stride = 2056
+    n_q = 8
+    sel = np.full((n_q, stride), -1, dtype=np.int32)
+    cnt = np.zeros(n_q, dtype=np.int32)
+    runs = [np.arange(0, 64), np.arange(65472, 65600), np.arange(131008, 131072),
+            np.arange(131072, 131105), np.arange(64, 128)[::3]]
+    for i in range(n_q):
+        cells = np.unique(np.concatenate([runs[(i + k) % len(runs)] for k in range(1 + i % 3)]))
+        sel[i, :len(cells)] = cells
+        cnt[i] = len(cells)
+    _compare(_gpu_union(qsa, sel, cnt), oracle.union_ref(sel, cnt))
