@@ -24,7 +24,9 @@
 //              TMEM only then), writes P = p * (V scale)
 //              as BF16 over its own S columns, and keeps its own FP32 sum of p.  At the
 //              end the pair adds their sums and each stores half of O's columns.
-//              They also write the Q rows into the shared-memory Q tile first.
+//              They also write the Q rows, as FP16, into the shared-memory Q tile
+//              first (a row outside FP16's comfortable range is stored times an
+//              exact power of two that the scores undo).
 //   warp 3     producer: union entries -> page table -> per-chunk tables in an
 //              8-deep ring (pool row of each cell, K/V scales, one 64-bit
 //              selection mask per query built with warp ballots), three chunks
@@ -32,22 +34,26 @@
 //              well before the loaders gather them.  Also zeroes the Q tile's pad
 //              rows.
 //   warp 7     MMA issuer (one thread), per chunk t: S(t) = Q K^T (A = Q tile,
-//              B = K tile, M=128 N=64 K=128) into S buffer t & 1, then
-//              O += P(t-1) V (A = P from TMEM, B = V tile, M=128 N=128 K=64).
+//              B = K tile, FP16, M=128 N=64 K=128) into S buffer t & 1, then
+//              O += P(t-1) V (A = P from TMEM, B = V tile, BF16, M=128 N=128 K=64).
 //              S is double-buffered, so S(t) runs while the softmax warps work
 //              on chunk t-1.  (A tcgen05.mma with M=128, K=16 costs the same ~46
 //              cycles for any N up to 64 and reaches full rate at N=128, so S is
 //              issued 64 columns wide.)
-//   warps 8-11 loaders/converters: 16-byte loads of the INT8 K rows (issued one
-//              chunk ahead into registers) and V rows (issued before the chunk's
-//              K conversion), converted to BF16 straight into operand tiles in
-//              the 128-byte swizzled layouts the tensor core reads,
-//              double-buffered; a K tile is refilled once S has read it, a V tile
-//              once P V has.  K and V stay exact (|int8| <= 128 fits BF16): the
-//              K scale multiplies the score column in FP32, so the logits carry
-//              no BF16 rounding, and the V scale multiplies p before P is
-//              rounded to BF16, so each product term is rounded once.
+//   warps 8-11 loaders/converters: one 16-byte load per row and thread of the
+//              INT8 K rows (issued one chunk ahead into registers) and V rows
+//              (issued before the chunk's K conversion), converted straight into
+//              operand tiles in the 128-byte swizzled layouts the tensor core
+//              reads -- K to FP16, V to BF16 -- double-buffered; a K tile is
+//              refilled once S has read it, a V tile once P V has.  K and V stay
+//              exact (|int8| <= 128 fits both formats): the K scale multiplies
+//              the score column in FP32, so the logits carry no 16-bit rounding,
+//              and the V scale multiplies p before P is rounded to BF16, so each
+//              product term is rounded once.
 // Rows 96-127 of the M=128 tiles are padding (Q rows zero, never stored).
+// The MMA thread commits three barriers per chunk: S_FULL[b] (S buffer b full,
+// and K tile b free), V_EMPTY[b] (P V done: V tile b free, and O may be
+// rescaled) and, once, O_DONE.
 // TMEM (256 columns): S/P buffers [0,64) and [64,128), O [128,256).  In S
 // buffer b, P of columns [0,32) goes to [b*64, b*64+16) and P of columns
 // [32,64) to [b*64+32, b*64+48): each softmax warp overwrites only S columns it
