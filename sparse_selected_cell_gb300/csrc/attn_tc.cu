@@ -141,11 +141,25 @@ __device__ __forceinline__ bool wait_addr(const Ctx& c, uint32_t addr, uint32_t 
 }
 
 // Barrier among the 64 threads of the two softmax warps that own lane quadrant q
-// (named barriers 1-3; immediate ids keep the kernel's barrier count at 4).
-__device__ __forceinline__ void pair_sync(int q) {
+// (named barriers 1-3; immediate ids keep the kernel's barrier count at 4).  A
+// named barrier cannot time out, so after an abort a warp never waits on one: it
+// checks the CTA's abort flag first and returns false, and every softmax exit
+// after a failed wait or a false pair_sync adds this warp's share with a
+// non-blocking arrive (pair_leave).  Both warps pass the same barriers in the
+// same order, so the partner is then either released from the barrier it is
+// waiting on or sees the flag at its next one.  (`aborted` is the flag as read
+// after this warp's previous pair barrier, which is all the argument needs.)
+__device__ __forceinline__ bool pair_sync(int q, bool aborted) {
+    if (aborted) return false;
     if (q == 0) asm volatile("bar.sync 1, 64;" ::: "memory");
     else if (q == 1) asm volatile("bar.sync 2, 64;" ::: "memory");
     else asm volatile("bar.sync 3, 64;" ::: "memory");
+    return true;
+}
+__device__ __forceinline__ void pair_leave(int q) {
+    if (q == 0) asm volatile("bar.arrive 1, 64;" ::: "memory");
+    else if (q == 1) asm volatile("bar.arrive 2, 64;" ::: "memory");
+    else asm volatile("bar.arrive 3, 64;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ producer
@@ -571,9 +585,15 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         // the row's largest |q| over both halves (row-sum slots: not used again before the end)
         float* xl = xchg + 4 * kRows;
         xl[hf * kRows + r] = amax;
-        pair_sync(quad);
+        if (!pair_sync(quad, *c.abort_flag != 0)) {
+            pair_leave(quad);
+            return;
+        }
         amax = fmaxf(amax, xl[(hf ^ 1) * kRows + r]);
-        pair_sync(quad);   // both have read before either writes a row sum there
+        if (!pair_sync(quad, *c.abort_flag != 0)) {   // both have read before either writes a row sum there
+            pair_leave(quad);
+            return;
+        }
         const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127;   // floor(log2 amax)
         // |e| <= 114, so 2^e and 2^-e are normal floats
         const int e = (amax > 0.f && (ex >= 14 || ex < -10)) ? min(max(ex - 12, -114), 114) : 0;
@@ -604,6 +624,7 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < c.n_chunks; ++t) {
+        const bool aborted = *c.abort_flag != 0;   // read after the previous pair barrier
         const int sb = t & 1, ts = t % kNS;
         const uint32_t tS = c.tmem + lane_base + kColS + 64 * sb;
         if (!(ok = wait_addr(c, bar(c, BAR_TAB_FULL + ts), (t / kNS) & 1))) break;   // the chunk's tables
@@ -630,7 +651,7 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
         // swap half-chunk maxima with the partner warp, so both take the same step
         float* xb = xchg + (t & 1) * (2 * kRows);
         xb[hf * kRows + r] = fmaxf(mx, my);
-        pair_sync(quad);
+        if (!(ok = pair_sync(quad, aborted))) break;
         const float m_new = fmax3(m, fmaxf(mx, my), xb[(hf ^ 1) * kRows + r]);
         const bool need = (m != -INFINITY) && (m_new > m + thresh);
         const float m_use = (m == -INFINITY || need) ? m_new : m;
@@ -685,11 +706,17 @@ __device__ void softmax_role(const Ctx& c, int hf, int quad, int lane) {
             for (int v = 0; v < 16; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    if (!ok) return;
+    if (!ok) {
+        pair_leave(quad);
+        return;
+    }
     // total weight of the row: this warp's sum plus the partner's
     float* xl = xchg + 4 * kRows;
     xl[hf * kRows + r] = l;
-    pair_sync(quad);
+    if (!pair_sync(quad, *c.abort_flag != 0)) {
+        pair_leave(quad);
+        return;
+    }
     const float l_tot = l + xl[(hf ^ 1) * kRows + r];
     if (!wait_addr(c, bar(c, BAR_O_DONE), 0)) return;
     tc::fence_after_sync();
