@@ -68,6 +68,8 @@ def parse():
     p.add_argument("--variant", type=int, default=0, help="0 default, 1 tcgen05, 2 mma.sync, 3 tcgen05 wide")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--decode", action="store_true",
+                   help="time decode over a batch of sequences (qsa_decode_attn) instead of the prompt chunk")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--drift-sweep", type=str, default=None,
                    help="comma-separated drift values: one line per value with the union ratio, the "
@@ -282,12 +284,60 @@ def drift_sweep(args):
                           "status": int(st.item())}), flush=True)
 
 
+def decode_bench(args):
+    """Decode over a batch of sequences (qsa_decode_attn): one query per sequence,
+    each with its own page table into one shared 1 GB pool (far above L2), timed
+    with CUDA events; one JSON line, separate from the prompt-chunk headline."""
+    import torch
+    from sparse_selected_cell_gb300 import build as qbuild
+    from sparse_selected_cell_gb300 import gen, qsa
+    torch.cuda.set_device(0)
+    qbuild.build()
+    w = gen.make_decode(**gen.DECODE_BENCH)
+
+    def dev(x):
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    q, kp, vp = dev(w.q), dev(w.k_pool), dev(w.v_pool)
+    ks, vs = dev(w.k_scale.view(np.int16)), dev(w.v_scale.view(np.int16))
+    pts, sel, cnt = dev(w.page_tables), dev(w.sel), dev(w.sel_count)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.empty((w.n_seq, w.n_heads, 128), dtype=torch.float32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    for _ in range(args.warmup):
+        qsa.decode_attn(q, kp, vp, ks, vs, pts, sel, cnt, out=out, dev_status=st)
+    torch.cuda.synchronize()
+    ev[0].record()
+    for _ in range(args.steps):
+        qsa.decode_attn(q, kp, vp, ks, vs, pts, sel, cnt, out=out, dev_status=st)
+    ev[1].record()
+    torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    hbm, _, _, src = peaks()
+    resident = w.page_tables[np.arange(w.n_seq)[:, None], np.where(w.sel >= 0, w.sel >> 6, 0)] >= 0
+    cells = int((resident & (np.arange(w.sel.shape[1])[None, :] < w.sel_count[:, None])).sum())
+    alg = cells * w.n_kv * 260 + w.n_seq * w.n_heads * 128 * 6
+    achieved = alg / (ms / 1e3) / 1e9
+    print(json.dumps({"mode": "decode", "metric": "decode query-head rows/s", "unit": "query-head rows/s",
+                      "value": w.n_seq * w.n_heads / (ms / 1e3), "ms_per_step": ms, "steps": args.steps,
+                      "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+                      "config": {"workload": f"decode: {w.n_seq:,} sequences x {w.ctx:,} cells, {w.n_kv} KV heads "
+                                             f"x 12, one query per sequence, page tables into a shared pool of "
+                                             f"{w.n_ppages:,} pages", "l2": "pool of %.2f GB, above L2"
+                                             % ((w.k_pool.nbytes + w.v_pool.nbytes) / 1e9)},
+                      "roofline": {"bound": "hbm", "kernel": "select_attn_kernel", "achieved": achieved, "peak": hbm,
+                                   "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
+                                   "algorithmic_bytes_per_launch": alg},
+                      "status": int(st.item())}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.drift_sweep:
         return drift_sweep(args)
+    if args.decode:
+        return decode_bench(args)
 
     import torch
     from sparse_selected_cell_gb300 import build as qbuild

@@ -151,6 +151,29 @@ int qsa_select_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
                     float sm_scale, float* out, int32_t* dev_status, void* stream);
 
+/* Decode-time selected-cell attention over a batch of sequences: query i is the
+ * current position of sequence i and attends to its own selected cells through
+ * its own page table.  The union pages leave decode untouched ("sycl: prompt
+ * attention over 8-query selection unions on XMX", Strata PR #2808, section
+ * Summary: the decode kernel gathers each position's own cells); this is that
+ * computation -- the softmax of qsa_select_attn, per query -- with one page table
+ * per query instead of one for the whole chunk.
+ *   - q: [n_q][n_kv*12][128] BF16; out: [n_q][n_kv*12][128] FP32, written for
+ *     every query (zeros when no selected cell is resident).
+ *   - page_tables: query i's table is page_tables[i * pt_stride ...], n_lpages
+ *     entries (logical page -> physical page in the shared pools, < 0 = not
+ *     resident).  pt_stride == 0 gives every query one shared table (then this
+ *     is qsa_select_attn); otherwise pt_stride >= n_lpages.
+ *   - Pools, scales, sel / sel_count / sel_stride, sm_scale, dev_status and
+ *     stream as in qsa_select_attn; lists need not be sorted.
+ *   - Returns QSA_ERR_ARG for a negative pt_stride or 0 < pt_stride < n_lpages,
+ *     otherwise as qsa_select_attn.  n_q == 0 returns QSA_OK with no launch. */
+int qsa_decode_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
+                    const uint16_t* k_scale, const uint16_t* v_scale,
+                    const int32_t* page_tables, int32_t pt_stride, int32_t n_lpages, int32_t n_ppages,
+                    int32_t n_kv, const int32_t* sel, const int32_t* sel_count, int32_t sel_stride,
+                    int32_t n_q, float sm_scale, float* out, int32_t* dev_status, void* stream);
+
 /* Bytes of the static device scratch behind qsa_prompt_attn_static (32 MiB):
  * room for n_q <= 3256 queries at union_stride 16448, more at smaller strides. */
 #define QSA_STATIC_SCRATCH_BYTES (32u << 20)

@@ -144,7 +144,22 @@ int qsa_select_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
     if (n_q == 0) return QSA_OK;
     if (!sel || !sel_count) return QSA_ERR_ARG;
     const qsa::SelArgs a{q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv,
-                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status};
+                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status, 0};
+    return cuda_status(qsa::launch_select_attn(a, static_cast<cudaStream_t>(stream)));
+}
+
+int qsa_decode_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool, const uint16_t* k_scale,
+                    const uint16_t* v_scale, const int32_t* page_tables, int32_t pt_stride, int32_t n_lpages,
+                    int32_t n_ppages, int32_t n_kv, const int32_t* sel, const int32_t* sel_count, int32_t sel_stride,
+                    int32_t n_q, float sm_scale, float* out, int32_t* dev_status, void* stream) {
+    int rc = check_attn_args(q, k_pool, v_pool, k_scale, v_scale, page_tables, n_lpages, n_ppages, n_kv, n_q, out,
+                             QSA_ATTN_DEFAULT);
+    if (rc != QSA_OK) return rc;
+    if (sel_stride <= 0 || pt_stride < 0 || (pt_stride > 0 && pt_stride < n_lpages)) return QSA_ERR_ARG;
+    if (n_q == 0) return QSA_OK;
+    if (!sel || !sel_count) return QSA_ERR_ARG;
+    const qsa::SelArgs a{q, k_pool, v_pool, k_scale, v_scale, page_tables, n_lpages, n_ppages, n_kv,
+                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status, pt_stride};
     return cuda_status(qsa::launch_select_attn(a, static_cast<cudaStream_t>(stream)));
 }
 

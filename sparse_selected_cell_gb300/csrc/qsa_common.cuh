@@ -142,14 +142,15 @@ cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_wide(const AttnArgs& a, cudaStream_t stream);
 
-// Per-position attention (no union): each query over its own selection list.
+// Per-position attention (no union): each query over its own selection list,
+// with one shared page table (prompt) or one table per query (decode).
 struct SelArgs {
     const uint16_t* q;
     const int8_t* k_pool;
     const int8_t* v_pool;
     const uint16_t* k_scale;
     const uint16_t* v_scale;
-    const int32_t* page_table;
+    const int32_t* page_table;   // query i's table: page_table + i * pt_stride (0: one shared table)
     int n_lpages, n_ppages, n_kv;
     const int32_t* sel;
     const int32_t* sel_count;
@@ -157,6 +158,7 @@ struct SelArgs {
     float sm_scale;
     float* out;
     int32_t* dev_status;
+    int pt_stride;
 };
 
 cudaError_t launch_select_attn(const SelArgs& a, cudaStream_t stream);

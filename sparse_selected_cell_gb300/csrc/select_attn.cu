@@ -8,7 +8,9 @@
 // Extra Notes times it against the union kernel at several union ratios.  The
 // result is the same per-position softmax the union path computes; here it runs
 // on the warp-level tensor path so that the comparison is between data-movement
-// strategies, not between FP32 and tensor cores.
+// strategies, not between FP32 and tensor cores.  The same kernel serves decode
+// over a batch of sequences (qsa_decode_attn): query i is sequence i's current
+// position, with its own page table at page_table + i * pt_stride.
 //
 // One warp per (query position i, KV head h): its 12 query heads are rows 0-11
 // of one m16 tile (rows 12-15 padding), Q held as A fragments in registers.  The
@@ -85,6 +87,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
     }
     const int n_steps = (cnt + kStep - 1) / kStep;
     const int32_t* lst = a.sel + (size_t)i * a.sel_stride;
+    const int32_t* ptab = a.page_table + (size_t)i * a.pt_stride;   // this query's page table
 
     // ---- cell -> page -> row pipeline: lane l handles cell (l & 15) of a step, K (l < 16) or V (l >= 16)
     const int slot = lane & 15, kv = lane >> 4;
@@ -98,7 +101,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
             report(a.dev_status, QSA_DEV_BAD_CELL);
             return -1;
         }
-        const int pp = __ldg(a.page_table + (cell >> 6));
+        const int pp = __ldg(ptab + (cell >> 6));
         if (pp >= a.n_ppages) {
             report(a.dev_status, QSA_DEV_BAD_PAGE);
             return -1;

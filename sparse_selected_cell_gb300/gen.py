@@ -255,3 +255,76 @@ def make(config, seed: Optional[int] = None, nonresident_frac: float = 0.0,
                     n_lpages=n_lpages, n_ppages=n_ppages, drift=float(cfg["drift"]), seed=s,
                     q=q, k_pool=k, v_pool=v, k_scale=ks, v_scale=vs, page_table=pt,
                     sel=sel, sel_count=cnt)
+
+
+# The decode workload the benchmark times (`bench.py --decode`): 1,024 sequences
+# of 32,768 cells, 4 KV heads, pages drawn from a shared pool of 16,384 pages
+# (1 GB of INT8 K and V, far above L2).
+DECODE_BENCH = dict(n_seq=1024, ctx=32768, n_kv=4, n_ppages=16384, seed=11)
+
+
+@dataclasses.dataclass
+class DecodeWorkload:
+    """One synthetic decode step over a batch of sequences.  Host numpy arrays.
+
+    q           uint16 [n_seq, n_kv*12, 128]   BF16 bit patterns, one query per sequence
+    k_pool ...  as in Workload, [n_ppages, n_kv, 64, 128] (shared by all sequences)
+    page_tables int32  [n_seq, n_lpages]       sequence i's logical page -> physical page
+    sel         int32  [n_seq, sel_stride]     sequence i's selection at its last position
+    sel_count   int32  [n_seq]
+    Every sequence holds ctx cells; its query sits at position ctx - 1.
+    """
+    ctx: int
+    n_seq: int
+    n_kv: int
+    n_lpages: int
+    n_ppages: int
+    seed: int
+    q: np.ndarray
+    k_pool: np.ndarray
+    v_pool: np.ndarray
+    k_scale: np.ndarray
+    v_scale: np.ndarray
+    page_tables: np.ndarray
+    sel: np.ndarray
+    sel_count: np.ndarray
+
+    @property
+    def n_heads(self) -> int:
+        return self.n_kv * HEADS_PER_KV
+
+    @property
+    def sm_scale(self) -> float:
+        return 1.0 / math.sqrt(HEAD_DIM)
+
+
+def make_decode(n_seq: int, ctx: int, n_kv: int, n_ppages: int, seed: int, nonresident_frac: float = 0.0,
+                scale_lo: float = 0.01, scale_hi: float = 0.03, q_sigma: float = 1.0) -> DecodeWorkload:
+    """A decode batch: n_seq sequences of ctx cells whose pages are drawn, each
+    sequence without repeats, from one shared pool of n_ppages physical pages (so
+    sequences may share pages, as prefix-sharing sequences do); each query selects
+    by the block recipe at its position ctx - 1 (sinks, the local window and 24 of
+    a 32-block pool; no drift: one position per sequence).  A fraction of every
+    table may be marked not resident."""
+    n_lpages = (ctx + PAGE_CELLS - 1) // PAGE_CELLS
+    if n_lpages > n_ppages:
+        raise ValueError("a sequence needs more pages than the pool holds")
+    rng_pt = _rng(seed, _STREAM_PT)
+    pts = np.empty((n_seq, n_lpages), dtype=np.int32)
+    for i in range(n_seq):
+        pts[i] = rng_pt.choice(n_ppages, size=n_lpages, replace=False).astype(np.int32)
+    if nonresident_frac > 0.0:
+        off = _rng(seed, _STREAM_RES).random(size=pts.shape) < nonresident_frac
+        pts[off] = -1
+    rng_sel = _rng(seed, _STREAM_SEL)
+    sel = np.full((n_seq, SEL_STRIDE), -1, dtype=np.int32)
+    cnt = np.zeros(n_seq, dtype=np.int32)
+    for i in range(n_seq):
+        s1, c1 = block_selection(ctx - 1, 1, 0.0, rng_sel)
+        sel[i] = s1[0]
+        cnt[i] = c1[0]
+    k, v, ks, vs = make_pool(n_ppages, n_kv, scale_lo, scale_hi, seed)
+    q = make_q(n_seq, n_kv * HEADS_PER_KV, q_sigma, seed)
+    return DecodeWorkload(ctx=ctx, n_seq=n_seq, n_kv=n_kv, n_lpages=n_lpages, n_ppages=n_ppages, seed=seed,
+                          q=q, k_pool=k, v_pool=v, k_scale=ks, v_scale=vs, page_tables=pts, sel=sel,
+                          sel_count=cnt)

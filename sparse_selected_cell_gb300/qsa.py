@@ -58,6 +58,8 @@ def lib():
         L.qsa_prompt_attn_static.restype = ctypes.c_int
         L.qsa_select_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
         L.qsa_select_attn.restype = ctypes.c_int
+        L.qsa_decode_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
+        L.qsa_decode_attn.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -191,6 +193,40 @@ def select_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
                                int(page_table.shape[0]), int(k_pool.shape[0]), n_kv, _ptr(sel), _ptr(sel_count),
                                int(sel.shape[1]), n_q, float(sm_scale), _ptr(out), _ptr(dev_status), _stream(stream))
     _check("qsa_select_attn", rc)
+    return out
+
+
+def decode_attn(q, k_pool, v_pool, k_scale, v_scale, page_tables, sel, sel_count,
+                sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                dev_status: Optional[torch.Tensor] = None, stream=None,
+                n_lpages: Optional[int] = None) -> torch.Tensor:
+    """Decode over a batch of sequences (qsa_decode_attn): page_tables int32 [n_q, width], one table per
+    query (the first n_lpages entries of its row; n_lpages defaults to the width, which is the stride)
+    -> out float32 [n_q, n_kv*12, 128]."""
+    _dev(q, "q", _B16)
+    _dev(k_pool, "k_pool", (torch.int8,))
+    _dev(v_pool, "v_pool", (torch.int8,))
+    _dev(k_scale, "k_scale", _H16)
+    _dev(v_scale, "v_scale", _H16)
+    _dev(page_tables, "page_tables", (torch.int32,))
+    _dev(sel, "sel", (torch.int32,))
+    _dev(sel_count, "sel_count", (torch.int32,))
+    n_q, n_heads = int(q.shape[0]), int(q.shape[1])
+    if page_tables.dim() != 2 or int(page_tables.shape[0]) != n_q or not page_tables.is_contiguous():
+        raise ValueError("page_tables must be a contiguous [n_q, width] array")
+    n_kv = n_heads // gen.HEADS_PER_KV
+    if out is None:
+        out = torch.empty((n_q, n_heads, gen.HEAD_DIM), dtype=torch.float32, device=q.device)
+    _dev(out, "out", (torch.float32,))
+    if sm_scale is None:
+        sm_scale = gen.HEAD_DIM ** -0.5
+    rc = lib().qsa_decode_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(page_tables),
+                               int(page_tables.shape[1]),
+                               int(page_tables.shape[1]) if n_lpages is None else int(n_lpages),
+                               int(k_pool.shape[0]), n_kv,
+                               _ptr(sel), _ptr(sel_count), int(sel.shape[1]), n_q, float(sm_scale), _ptr(out),
+                               _ptr(dev_status), _stream(stream))
+    _check("qsa_decode_attn", rc)
     return out
 
 

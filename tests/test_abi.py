@@ -79,3 +79,17 @@ def test_prompt_attn_capacity(lib):
     rc = lib.qsa_prompt_attn(fake, fake, fake, fake, fake, fake, 1, 1, 1, fake, fake, 2056, 8, ctypes.c_float(0.088),
                              fake, fake, ctypes.c_size_t(1024), 16448, 0, None, None)
     assert rc == 3  # QSA_ERR_CAPACITY: workspace smaller than qsa_union_workspace_bytes
+
+
+def test_decode_host_argument_checks(lib):
+    ERR_ARG = 1
+    fake = ctypes.c_void_p(0x100000)
+    f = ctypes.c_float(0.088)
+
+    def dec(pt_stride, n_lpages=4, n_q=8, sel_stride=2056):
+        return lib.qsa_decode_attn(fake, fake, fake, fake, fake, fake, pt_stride, n_lpages, 16, 1, fake, fake,
+                                   sel_stride, n_q, f, fake, None, None)
+    assert dec(4, n_q=0) == 0                 # nothing to do, no launch
+    assert dec(-1) == ERR_ARG                 # negative page-table stride
+    assert dec(3) == ERR_ARG                  # tables would overlap: 0 < pt_stride < n_lpages
+    assert dec(4, sel_stride=0) == ERR_ARG

@@ -89,3 +89,18 @@ def test_bf16_rounding_is_nearest_even():
     x = np.random.default_rng(0).standard_normal(100000).astype(np.float32)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(gen.f32_to_bf16_bits(x), ref)
+
+
+def test_make_decode_is_seeded_and_well_formed():
+    a = gen.make_decode(5, 4096, 2, 100, seed=3, nonresident_frac=0.2)
+    b = gen.make_decode(5, 4096, 2, 100, seed=3, nonresident_frac=0.2)
+    for x, y in ((a.q, b.q), (a.page_tables, b.page_tables), (a.sel, b.sel), (a.k_pool, b.k_pool)):
+        assert np.array_equal(x, y)
+    assert a.page_tables.shape == (5, 64) and a.q.shape == (5, 24, 128)
+    for i in range(a.n_seq):
+        row = a.page_tables[i]
+        live = row[row >= 0]
+        assert len(set(live.tolist())) == len(live) and (live < a.n_ppages).all()   # no repeats within a sequence
+        cells = a.sel[i, :a.sel_count[i]]
+        assert (np.diff(cells) > 0).all() and cells[0] == 0 and cells[-1] == a.ctx - 1   # sinks ... last position
+        assert a.sel_count[i] <= gen.CAP
