@@ -18,7 +18,8 @@
 //   * lanes 0-15 resolve cell -> page -> pool row for the K rows, lanes 16-31 for
 //     the V rows, in a three-step register pipeline (cells two steps ahead, the
 //     page table one step ahead), and issue 16-byte cp.async copies of the rows
-//     into a double-buffered INT8 stage (16-byte chunks XOR-swizzled by cell);
+//     into a 4-deep INT8 stage ring, three steps ahead of the step being
+//     computed (16-byte chunks XOR-swizzled by cell);
 //   * the warp converts the stage exactly to BF16 tiles (|int8| <= 127 fits
 //     BF16), S = Q K^T with mma.sync m16n8k16, the K scale (times sm_scale and
 //     log2 e) multiplies each score column in FP32, unselected / masked cells
@@ -32,22 +33,24 @@ namespace {
 constexpr int kSelWarps = 4;
 constexpr int kSelThreads = 32 * kSelWarps;
 constexpr int kStep = 16;                  // cells per step
+constexpr int kStages = 4;                 // INT8 stage ring: copies run kStages - 1 steps ahead
 constexpr float kSelRescaleLog2 = 32.f;    // lazy rescale threshold (exp2 domain), as in attn_tc.cu
 
 struct __align__(16) WarpSmem {
-    int8_t raw[2][2][kStep][kHeadDim];      // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   8 KB
+    int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   16 KB
     uint16_t kb[kStep][kHeadDim];           // BF16 K, 256-byte rows, 16-byte chunks XOR (cell & 7)   4 KB
     uint16_t vb[kStep][kHeadDim];           // BF16 V                                                4 KB
-    float ks[2][kStep];                     // K scale * sm_scale * log2(e); 0 for a masked cell
-    float vs[2][kStep];                     // V scale; 0 for a masked cell
-    uint32_t valid[2];                      // bit c: cell c of the step is selected and resident
+    float ks[kStages][kStep];               // K scale * sm_scale * log2(e); 0 for a masked cell
+    float vs[kStages][kStep];               // V scale; 0 for a masked cell
+    uint32_t valid[kStages];                // bit c: cell c of the step is selected and resident
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -70,7 +73,7 @@ __device__ __forceinline__ uint32_t swz(int cell, int chunk, int row_bytes) {
     return (uint32_t)(cell * row_bytes + ((chunk ^ (cell & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpSmem& s = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
@@ -125,12 +128,15 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         if (lane == 0) s.valid[st] = vm;
     };
 
-    int c1 = load_cell(1), c2 = load_cell(2);
-    {
-        const int c0 = load_cell(0);
-        issue(c0, resolve(c0), 0);
+    // prologue: copies of steps 0 .. kStages-2 in flight; then the register
+    // pipeline holds the cells of step kStages-1 (resolved) and kStages
+#pragma unroll 1
+    for (int k = 0; k < kStages - 1; ++k) {
+        const int c = load_cell(k);
+        issue(c, resolve(c), k);
+        cp_async_commit();
     }
-    cp_async_commit();
+    int c1 = load_cell(kStages - 1), c2 = load_cell(kStages);
     int p1 = resolve(c1);
 
     // ---- Q fragments (A operand): rows 0-11 are the KV head's 12 query heads
@@ -157,13 +163,14 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
 
 #pragma unroll 1
     for (int step = 0; step < n_steps; ++step) {
-        const int st = step & 1;
-        // pipeline: cells of step+3, page of step+2, copies of step+1
-        const int c3 = load_cell(step + 3);
+        const int st = step % kStages;
+        // pipeline: cells of step+kStages+1, page of step+kStages, copies of
+        // step+kStages-1 (into the stage step-1 used), while step's copies land
+        const int c3 = load_cell(step + kStages + 1);
         const int p2 = resolve(c2);
-        issue(c1, p1, st ^ 1);
+        issue(c1, p1, (step + kStages - 1) % kStages);
         cp_async_commit();
-        cp_async_wait1();
+        cp_async_wait<kStages - 1>();
         __syncwarp();
 
         // exact BF16 tiles: lane l converts 64 bytes (half l & 1) of cell (l >> 1) of K and of V
@@ -267,7 +274,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         c2 = c3;
         p1 = p2;
     }
-    cp_async_wait1();   // nothing left in flight when the warp exits (the last group is empty)
+    cp_async_wait<0>();   // nothing left in flight when the warp exits
 
     // ---- O / l for rows 0-11
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
