@@ -38,7 +38,7 @@ constexpr float kSelRescaleLog2 = 32.f;    // lazy rescale threshold (exp2 domai
 
 struct __align__(16) WarpSmem {
     int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   16 KB
-    uint16_t kb[kStep][kHeadDim];           // BF16 K, 256-byte rows, 16-byte chunks XOR (cell & 7)   4 KB
+    uint16_t kb[kStep][kHeadDim];           // BF16 K, 256-byte rows, 16-byte chunks swizzled (swz)   4 KB
     uint16_t vb[kStep][kHeadDim];           // BF16 V                                                4 KB
     float ks[kStages][kStep];               // K scale * sm_scale * log2(e); 0 for a masked cell
     float vs[kStages][kStep];               // V scale; 0 for a masked cell
@@ -68,9 +68,13 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// byte offset of 16-byte chunk `chunk` of a row `cell` of `row_bytes` bytes
+// byte offset of 16-byte chunk `chunk` (0-15) of the 256-byte BF16 row of `cell`.
+// The low three chunk bits are XORed with (cell & 7), so the 8 cells an ldmatrix
+// reads at one chunk hit 8 different bank groups; bit 3 of the chunk (which
+// 128-byte half) also flips bit 2, so the two lanes that store the two halves of
+// one cell's row in the same 8-lane phase hit different bank groups too.
 __device__ __forceinline__ uint32_t swz(int cell, int chunk, int row_bytes) {
-    return (uint32_t)(cell * row_bytes + ((chunk ^ (cell & 7)) << 4));
+    return (uint32_t)(cell * row_bytes + ((chunk ^ (cell & 7) ^ (((chunk >> 3) & 1) << 2)) << 4));
 }
 
 __global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelArgs a) {
