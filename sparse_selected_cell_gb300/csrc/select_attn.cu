@@ -18,7 +18,7 @@
 //   * lanes 0-15 resolve cell -> page -> pool row for the K rows, lanes 16-31 for
 //     the V rows, in a three-step register pipeline (cells two steps ahead, the
 //     page table one step ahead), and issue 16-byte cp.async copies of the rows
-//     into a 4-deep INT8 stage ring, three steps ahead of the step being
+//     into a 3-deep INT8 stage ring, two steps ahead of the step being
 //     computed (16-byte chunks XOR-swizzled by cell);
 //   * the warp converts the stage exactly to BF16 tiles (|int8| <= 127 fits
 //     BF16), S = Q K^T with mma.sync m16n8k16, the K scale (times sm_scale and
@@ -33,13 +33,13 @@ namespace {
 constexpr int kSelWarps = 4;
 constexpr int kSelThreads = 32 * kSelWarps;
 constexpr int kStep = 16;                  // cells per step
-constexpr int kStages = 4;                 // INT8 stage ring: copies run kStages - 1 steps ahead
+constexpr int kStages = 3;                 // INT8 stage ring: copies run kStages - 1 steps ahead
 constexpr float kSelRescaleLog2 = 32.f;    // lazy rescale threshold (exp2 domain), as in attn_tc.cu
 
 struct __align__(16) WarpSmem {
-    int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   16 KB
-    uint16_t kb[kStep][kHeadDim];           // BF16 K, 256-byte rows, 16-byte chunks swizzled (swz)   4 KB
-    uint16_t vb[kStep][kHeadDim];           // BF16 V                                                4 KB
+    int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   12 KB
+    uint16_t kb[kStep][kHeadDim];           // BF16 K, then V of the same step: 256-byte rows,      4 KB
+                                            // 16-byte chunks swizzled (swz)
     float ks[kStages][kStep];               // K scale * sm_scale * log2(e); 0 for a masked cell
     float vs[kStages][kStep];               // V scale; 0 for a masked cell
     uint32_t valid[kStages];                // bit c: cell c of the step is selected and resident
@@ -77,7 +77,7 @@ __device__ __forceinline__ uint32_t swz(int cell, int chunk, int row_bytes) {
     return (uint32_t)(cell * row_bytes + ((chunk ^ (cell & 7) ^ (((chunk >> 3) & 1) << 2)) << 4));
 }
 
-__global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpSmem& s = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelAr
 #pragma unroll
     for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const uint32_t kb_base = smem_u32(&s.kb[0][0]), vb_base = smem_u32(&s.vb[0][0]);
+    const uint32_t kb_base = smem_u32(&s.kb[0][0]), vb_base = kb_base;   // one tile: K, then V
 
 #pragma unroll 1
     for (int step = 0; step < n_steps; ++step) {
@@ -177,24 +177,23 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelAr
         cp_async_wait<kStages - 1>();
         __syncwarp();
 
-        // exact BF16 tiles: lane l converts 64 bytes (half l & 1) of cell (l >> 1) of K and of V
-        {
+        // exact BF16 tile (K first, then V in the same space): lane l converts 64
+        // bytes (half l & 1) of cell (l >> 1)
+        auto convert = [&](int tv) {
             const int cell = lane >> 1, hh = lane & 1;
+            uint8_t* dst = reinterpret_cast<uint8_t*>(&s.kb[0][0]);
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(&s.raw[st][tv][cell][0]);
 #pragma unroll
-            for (int tv = 0; tv < 2; ++tv) {
-                uint8_t* dst = reinterpret_cast<uint8_t*>(tv ? &s.vb[0][0] : &s.kb[0][0]);
-                const uint8_t* src = reinterpret_cast<const uint8_t*>(&s.raw[st][tv][cell][0]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int seg = 4 * hh + k;
-                    const uint4 x = *reinterpret_cast<const uint4*>(src + ((seg ^ (cell & 7)) << 4));
-                    uint4 lo, hi;
-                    int8x16_to_bf16(x, lo, hi);
-                    *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg, 256)) = lo;
-                    *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg + 1, 256)) = hi;
-                }
+            for (int k = 0; k < 4; ++k) {
+                const int seg = 4 * hh + k;
+                const uint4 x = *reinterpret_cast<const uint4*>(src + ((seg ^ (cell & 7)) << 4));
+                uint4 lo, hi;
+                int8x16_to_bf16(x, lo, hi);
+                *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg, 256)) = lo;
+                *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg + 1, 256)) = hi;
             }
-        }
+        };
+        convert(0);
         __syncwarp();
 
         // S = Q K^T: 16 rows x 16 cells
@@ -211,6 +210,8 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelAr
                 mma_bf16(sc[nt], qa[2 * kk2 + 1], b2, b3);
             }
         }
+        __syncwarp();   // every lane has read K out of the tile
+        convert(1);     // V into the same tile (read after the softmax below)
         // column scale (log2 domain), masked cells -inf
         const uint32_t vm = s.valid[st];
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -263,6 +264,7 @@ __global__ void __launch_bounds__(kSelThreads, 2) select_attn_kernel(const SelAr
         l0 = l0 * al0 + ps0;
         l1 = l1 * al1 + ps1;
         // O += P V: the 16 cells are one k16 step
+        __syncwarp();   // V is in the tile
         {
             const int cell = ((lane >> 3) & 1) * 8 + (lane & 7);
 #pragma unroll
