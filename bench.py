@@ -80,6 +80,11 @@ def parse():
     return p.parse_args()
 
 
+# GB300's nominal HBM3e bandwidth (~8 TB/s): the stricter denominator, reported
+# beside the measured copy bandwidth.
+NOMINAL_HBM_GBS = 8000.0
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -326,6 +331,7 @@ def decode_bench(args):
                                              % ((w.k_pool.nbytes + w.v_pool.nbytes) / 1e9)},
                       "roofline": {"bound": "hbm", "kernel": "select_attn_kernel", "achieved": achieved, "peak": hbm,
                                    "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
+                                   "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
                                    "algorithmic_bytes_per_launch": alg},
                       "status": int(st.item())}), flush=True)
 
@@ -495,6 +501,7 @@ def main():
             "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "kernel": kernel,
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "traffic": traffic, "peak_source": src,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
                          "algorithmic_bytes_per_launch": alg["bytes"], "flops_per_launch": alg["flops"],
                          "attn_ms": attn_avg, "tflops": tflops, "tensor_frac_sustained": tflops / bf16_sus,
                          "roofline_ms": max(t_hbm, t_tc), "union_build_ms": sum(union_ms) / len(union_ms),
