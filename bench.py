@@ -66,7 +66,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--variant", type=int, default=0, help="0 default, 1 tcgen05, 2 mma.sync, 3 tcgen05 wide")
-    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--decode", action="store_true",
                    help="time decode over a batch of sequences (qsa_decode_attn) instead of the prompt chunk")
