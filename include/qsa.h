@@ -174,6 +174,17 @@ int qsa_decode_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     int32_t n_kv, const int32_t* sel, const int32_t* sel_count, int32_t sel_stride,
                     int32_t n_q, float sm_scale, float* out, int32_t* dev_status, void* stream);
 
+/* Self-test of the bounded waits (not part of the method: the pages have no
+ * counterpart).  Every pipelined kernel here waits on mbarriers with a wall-time
+ * limit and, when one runs out, records QSA_DEV_WAIT_TIMEOUT in *dev_status and
+ * returns instead of hanging.  This launches one warp that waits on an mbarrier
+ * nothing arrives on, for limit_us microseconds, then records that bit: a test
+ * can see the whole path -- the wait ending by time, the device status reaching
+ * the host, the context staying usable -- without faulting anything.
+ *   - limit_us in (0, 10^7]; dev_status: device int32, OR-ed into, required.
+ *   - Returns QSA_ERR_ARG otherwise, QSA_ERR_CUDA if the launch fails. */
+int qsa_wait_selftest(int32_t limit_us, int32_t* dev_status, void* stream);
+
 /* Bytes of the static device scratch behind qsa_prompt_attn_static (32 MiB):
  * room for n_q <= 3256 queries at union_stride 16448, more at smaller strides. */
 #define QSA_STATIC_SCRATCH_BYTES (32u << 20)

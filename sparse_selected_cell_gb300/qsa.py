@@ -60,6 +60,8 @@ def lib():
         L.qsa_select_attn.restype = ctypes.c_int
         L.qsa_decode_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
         L.qsa_decode_attn.restype = ctypes.c_int
+        L.qsa_wait_selftest.argtypes = [_I, _P, _P]
+        L.qsa_wait_selftest.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -228,6 +230,12 @@ def decode_attn(q, k_pool, v_pool, k_scale, v_scale, page_tables, sel, sel_count
                                _ptr(dev_status), _stream(stream))
     _check("qsa_decode_attn", rc)
     return out
+
+
+def wait_selftest(limit_us: int, dev_status: torch.Tensor, stream=None) -> None:
+    """qsa_wait_selftest: one bounded wait that runs out after limit_us and sets QSA_DEV_WAIT_TIMEOUT."""
+    _dev(dev_status, "dev_status", (torch.int32,))
+    _check("qsa_wait_selftest", lib().qsa_wait_selftest(int(limit_us), _ptr(dev_status), _stream(stream)))
 
 
 STATIC_SCRATCH_BYTES = 32 << 20   # QSA_STATIC_SCRATCH_BYTES
