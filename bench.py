@@ -14,6 +14,13 @@ host->device inputs and device->host outputs inside the timed region.
 `cpu_baseline` times the FP64 CPU oracle on a bounded sample on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --config N            one of the five workloads (default 4)
+  python bench.py --all-configs         one line per workload 1-5
+  python bench.py <context> <queries> [reps] [--drift F] [--kv-heads H] [--seed S]
+                                        a custom chunk: the last <queries> positions of a
+                                        <context>-cell context, timed over [reps] steps
+  python bench.py --fused               time qsa_fused_attn (the union built inside the
+                                        attention CTA, one launch per step)
 """
 import argparse
 import hashlib
@@ -33,14 +40,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "query-head rows/sec at 40K ctx, 2,051-cell cap; achieved % of HBM roofline"
 UNIT = "query-head rows/s"
-CONFIG_ID = 4
+CONFIG_ID = 4   # the 40,960-cell context with an 8,192-position chunk: the headline workload
 
 
-def rank_seed(rank: int) -> int:
+def rank_seed(rank: int, config: int = CONFIG_ID) -> int:
     """Seed of rank `rank`'s chunk: every rank runs its own independent chunk of the
     same shape (weak scaling; the path has no exchange step between ranks)."""
     from sparse_selected_cell_gb300 import gen
-    return gen.CONFIGS[CONFIG_ID]["seed"] + 1000 * rank
+    return gen.CONFIGS[config]["seed"] + 1000 * rank
 
 
 def max_over_ranks(x: float, device) -> float:
@@ -61,11 +68,21 @@ def job_rows_per_s(world: int, rows_per_step: int, steps: int, ms: float) -> flo
 
 def parse():
     p = argparse.ArgumentParser()
+    p.add_argument("context", type=int, nargs="?", default=None, help="custom chunk: context length in cells")
+    p.add_argument("queries", type=int, nargs="?", default=None, help="custom chunk: query positions (the last ones)")
+    p.add_argument("reps", type=int, nargs="?", default=None, help="custom chunk: timed steps")
+    p.add_argument("--drift", type=float, default=None, help="selection drift (custom chunk; default 0.25)")
+    p.add_argument("--kv-heads", type=int, default=None, help="KV heads (custom chunk; default 4)")
+    p.add_argument("--seed", type=int, default=None, help="workload seed (custom chunk)")
+    p.add_argument("--config", type=int, default=CONFIG_ID, choices=[1, 2, 3, 4, 5])
+    p.add_argument("--all-configs", action="store_true", help="one line per workload 1-5")
+    p.add_argument("--fused", action="store_true", help="time qsa_fused_attn instead of the launch pair")
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--variant", type=int, default=0, help="0 default, 1 tcgen05, 2 mma.sync, 3 tcgen05 wide")
+    p.add_argument("--variant", type=int, default=0,
+                   help="0 default, 1 tcgen05 (two CTAs per SM), 2 tcgen05 (one CTA per SM)")
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--decode", action="store_true",
@@ -210,7 +227,7 @@ def run_reference(args):
     if rank != 0:
         return
     from sparse_selected_cell_gb300 import gen
-    w = gen.make(CONFIG_ID)
+    w = gen.make(args.config)
     n_steps = args.steps + args.warmup
     # size each step's sample so the whole run stays within about two minutes
     rate, n, dt, cores = oracle_sample(w, 0.5)
@@ -226,7 +243,9 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "oracle": "FP64 CPU oracle (OpenMP), per-position lists"},
+            "config": {"workload": workload_desc(w), "oracle": "FP64 CPU oracle (OpenMP), per-position lists",
+                       "sampled": f"each step times {per_step} of the workload's {w.n_q:,} query positions "
+                                  f"(consecutive, all {w.n_heads} heads); value is rows/s over those samples"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} consecutive query positions (all {w.n_heads} heads) per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -336,6 +355,208 @@ def decode_bench(args):
                       "status": int(st.item())}), flush=True)
 
 
+def custom_config(args, rank: int):
+    """The page's CLI shape: the last <queries> positions of a <context>-cell context
+    with the headline workload's value ranges."""
+    from sparse_selected_cell_gb300 import gen
+    cfg = dict(gen.CONFIGS[CONFIG_ID])
+    cfg.update(name=f"custom-ctx{args.context}-q{args.queries}", ctx=int(args.context), n_q=int(args.queries))
+    if args.kv_heads is not None:
+        cfg["n_kv"] = int(args.kv_heads)
+    if args.drift is not None:
+        cfg["drift"] = float(args.drift)
+    cfg["seed"] = (args.seed if args.seed is not None else cfg["seed"]) + 1000 * rank
+    return cfg
+
+
+def measure(args, w, dev, world: int, rank: int, headline: bool):
+    """Times one workload; returns rank 0's JSON line (None on other ranks)."""
+    import torch
+    from sparse_selected_cell_gb300 import gen, qsa
+
+    d = qsa.to_device(w, dev)
+    stream = torch.cuda.current_stream()
+    ws = torch.empty(qsa.workspace_bytes(w.n_q), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((w.n_q, w.n_heads, 128), dtype=torch.float32, device=dev)
+    n_groups = w.n_groups
+    stride = gen.UNION_STRIDE
+    cells_b = n_groups * stride * 4
+    mask_off = (cells_b + 255) // 256 * 256
+    cnt_off = mask_off + (n_groups * stride + 255) // 256 * 256
+    ucell = ws[:cells_b].view(torch.int32).view(n_groups, stride)
+    umask = ws[mask_off:mask_off + n_groups * stride].view(n_groups, stride)
+    ucount = ws[cnt_off:cnt_off + n_groups * 4].view(torch.int32)
+    # the union counts for the algorithmic bytes come from the launch pair's union build
+    qsa.union_build(d["sel"], d["sel_count"], stride, out=(ucell, umask, ucount), dev_status=status, stream=stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if args.fused:
+            if ev is not None:
+                ev[1].record(stream)
+            qsa.fused_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"], d["sel"],
+                           d["sel_count"], out=out, dev_status=status, stream=stream)
+        else:
+            qsa.union_build(d["sel"], d["sel_count"], stride, out=(ucell, umask, ucount), dev_status=status,
+                            stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            qsa.union_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"], ucell,
+                           umask, ucount, out=out, variant=args.variant, dev_status=status, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
+    alg = algorithmic(w, ucount.cpu().numpy())
+    steps = args.steps
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    bus = None
+    try:
+        bus = torch.cuda.get_device_properties(dev).pci_bus_id
+    except Exception:
+        pass
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(bus) as clk:
+        t0.record(stream)
+        for k in range(steps):
+            step(evs[k])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    union_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    total_ms = max_over_ranks(total_ms, dev)
+    rows_per_step = w.n_q * w.n_heads
+    value = job_rows_per_s(world, rows_per_step, steps, total_ms)
+
+    # End to end through the public call: every step copies all of its inputs from
+    # pinned host memory and reads its output back to pinned host memory.  Steps run
+    # as a serving loop would run them: host-to-device copies, compute and
+    # device-to-host copies on three streams, over two device buffer sets, so step
+    # k+1's inputs travel while step k computes and step k-1's output travels back.
+    e2e_steps = args.e2e_steps if headline else 0
+    host = {k: v.cpu().pin_memory() for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+    e2e_ms = float("nan")
+    if e2e_steps > 0:
+        host_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        bufs = [{k: torch.empty_like(v) for k, v in d.items()} for _ in range(2)]
+        outs = [out, torch.empty_like(out)]
+        wss = [ws, torch.empty_like(ws)]
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+        def e2e_step(k):
+            b = k % 2
+            s_in.wait_event(ev_cmp[b])                 # step k-2 is done reading buffer set b
+            with torch.cuda.stream(s_in):
+                for name, v in host.items():
+                    bufs[b][name].copy_(v, non_blocking=True)
+            ev_in[b].record(s_in)
+            s_cmp.wait_event(ev_in[b])
+            s_cmp.wait_event(ev_out[b])                # step k-2's output has been read back
+            dd = bufs[b]
+            if args.fused:
+                qsa.fused_attn(dd["q"], dd["k_pool"], dd["v_pool"], dd["k_scale"], dd["v_scale"], dd["page_table"],
+                               dd["sel"], dd["sel_count"], out=outs[b], dev_status=status, stream=s_cmp)
+            else:
+                qsa.prompt_attn(dd["q"], dd["k_pool"], dd["v_pool"], dd["k_scale"], dd["v_scale"], dd["page_table"],
+                                dd["sel"], dd["sel_count"], out=outs[b], workspace=wss[b], variant=args.variant,
+                                dev_status=status, stream=s_cmp)
+            ev_cmp[b].record(s_cmp)
+            s_out.wait_event(ev_cmp[b])
+            with torch.cuda.stream(s_out):
+                host_outs[b].copy_(outs[b], non_blocking=True)
+            ev_out[b].record(s_out)
+
+        for k in range(3):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        e1.record(s_out)                           # after the last read-back, which follows everything
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = job_rows_per_s(world, rows_per_step, e2e_steps, e2e_ms) if e2e_steps > 0 else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
+    if rank != 0:
+        return None
+
+    hbm, bf16, bf16_sus, src = peaks()
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    abytes = alg["bytes"]
+    if args.fused:   # the fused kernel reads each group's lists (once per KV head) instead of the union arrays
+        abytes = alg["bytes"] - int(ucount.cpu().numpy().astype(np.int64).sum()) * w.n_kv * 5 \
+            + int(w.sel_count.astype(np.int64).sum()) * 4 * w.n_kv
+    achieved = abytes / (attn_avg / 1e3) / 1e9
+    tflops = alg["flops"] / (attn_avg / 1e3) / 1e12
+    t_hbm = abytes / (hbm * 1e9) * 1e3
+    t_tc = alg["flops"] / (bf16_sus * 1e12) * 1e3
+    resolved = args.variant or qsa.default_variant()
+    if args.fused:
+        kernel, files, vname = "attn_sm_kernel", ("attn_sm.cu", "tc_ptx.cuh"), "fused (union built in the CTA)"
+    else:
+        kernel, files = {qsa.ATTN_TCGEN05: ("attn_tc_kernel", ("attn_tc.cu", "tc_ptx.cuh")),
+                         qsa.ATTN_TCGEN05_SM: ("attn_sm_kernel", ("attn_sm.cu", "tc_ptx.cuh"))}[resolved]
+        vname = {1: "tcgen05, two CTAs per SM", 2: "tcgen05, one CTA per SM"}[resolved]
+    srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in files + ("qsa_common.cuh",)]
+    traffic, digest = read_traffic(kernel, srcs)
+    in_bytes = sum(v.numel() * v.element_size() for v in d.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(w),
+                   "l2": "inputs above L2 (%.0f MB read + %.0f MB written per step), so no step starts with "
+                         "them in L2; the 42.6 MB KV pool itself is gathered ~2.7x per launch and stays "
+                         "L2-resident within a launch (DRAM traffic / algorithmic bytes below)"
+                         % (in_bytes / 1e6, out.numel() * 4 / 1e6),
+                   "mean_union_cells": round(alg["mean_union"], 1), "union_ratio": round(alg["union_ratio"], 3),
+                   "variant": vname, "parallelism": f"dp{world}"},
+        "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "kernel": kernel,
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": traffic,
+                     "traffic_over_algorithmic": (traffic / abytes) if traffic else None,
+                     "peak_source": src,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                     "algorithmic_bytes_per_launch": abytes, "flops_per_launch": alg["flops"],
+                     "attn_ms": attn_avg, "tflops": tflops, "tensor_frac_sustained": tflops / bf16_sus,
+                     "roofline_ms": max(t_hbm, t_tc),
+                     "union_build_ms": None if args.fused else sum(union_ms) / len(union_ms),
+                     "source_sha256_16": digest},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps,
+                "pipeline": "copy-in, compute and copy-out streams over two buffer sets"},
+        "gpu_launches": (1 if args.fused else 2) * steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        rate, n, dt, cores = oracle_sample(w, args.cpu_seconds if headline else min(args.cpu_seconds, 4.0))
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{n} consecutive query positions x {w.n_heads} heads of the same "
+                                          f"chunk ({dt:.1f} s, FP64, OpenMP)"}
+    return line
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -366,158 +587,23 @@ def main():
     qsa.lib()
 
     # every rank runs its own independent chunk of the same shape (weak scaling)
-    w = gen.make(CONFIG_ID, seed=rank_seed(rank), n_q=args.n_q)
-    d = qsa.to_device(w, dev)
-    stream = torch.cuda.current_stream()
-    ws = torch.empty(qsa.workspace_bytes(w.n_q), dtype=torch.uint8, device=dev)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    out = torch.empty((w.n_q, w.n_heads, 128), dtype=torch.float32, device=dev)
-    n_groups = w.n_groups
-    stride = gen.UNION_STRIDE
-    cells_b = n_groups * stride * 4
-    mask_off = (cells_b + 255) // 256 * 256
-    cnt_off = mask_off + (n_groups * stride + 255) // 256 * 256
-    ucell = ws[:cells_b].view(torch.int32).view(n_groups, stride)
-    umask = ws[mask_off:mask_off + n_groups * stride].view(n_groups, stride)
-    ucount = ws[cnt_off:cnt_off + n_groups * 4].view(torch.int32)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        qsa.union_build(d["sel"], d["sel_count"], stride, out=(ucell, umask, ucount), dev_status=status, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        qsa.union_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"], ucell, umask,
-                       ucount, out=out, variant=args.variant, dev_status=status, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
-    alg = algorithmic(w, ucount.cpu().numpy())
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    bus = None
-    try:
-        bus = torch.cuda.get_device_properties(dev).pci_bus_id
-    except Exception:
-        pass
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(bus) as clk:
-        t0.record(stream)
-        for k in range(args.steps):
-            step(evs[k])
-        t1.record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = t0.elapsed_time(t1)
-    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    union_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    total_ms = max_over_ranks(total_ms, dev)
-    rows_per_step = w.n_q * w.n_heads
-    value = job_rows_per_s(world, rows_per_step, args.steps, total_ms)
-
-    # End to end through the public call: every step copies all of its inputs from
-    # pinned host memory and reads its output back to pinned host memory.  Steps run
-    # as a serving loop would run them: host-to-device copies, compute and
-    # device-to-host copies on three streams, over two device buffer sets, so step
-    # k+1's inputs travel while step k computes and step k-1's output travels back.
-    host = {k: v.cpu().pin_memory() for k, v in d.items()}
-    host_outs = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-    bufs = [{k: torch.empty_like(v) for k, v in d.items()} for _ in range(2)]
-    outs = [out, torch.empty_like(out)]
-    wss = [ws, torch.empty_like(ws)]
-    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-    ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = host_outs[0].numel() * host_outs[0].element_size()
-
-    def e2e_step(k):
-        b = k % 2
-        s_in.wait_event(ev_cmp[b])                 # step k-2 is done reading buffer set b
-        with torch.cuda.stream(s_in):
-            for name, v in host.items():
-                bufs[b][name].copy_(v, non_blocking=True)
-        ev_in[b].record(s_in)
-        s_cmp.wait_event(ev_in[b])
-        s_cmp.wait_event(ev_out[b])                # step k-2's output has been read back
-        dd = bufs[b]
-        qsa.prompt_attn(dd["q"], dd["k_pool"], dd["v_pool"], dd["k_scale"], dd["v_scale"], dd["page_table"],
-                        dd["sel"], dd["sel_count"], out=outs[b], workspace=wss[b], variant=args.variant,
-                        dev_status=status, stream=s_cmp)
-        ev_cmp[b].record(s_cmp)
-        s_out.wait_event(ev_cmp[b])
-        with torch.cuda.stream(s_out):
-            host_outs[b].copy_(outs[b], non_blocking=True)
-        ev_out[b].record(s_out)
-
-    e2e_ms = float("nan")
-    if args.e2e_steps > 0:
-        for k in range(3):
-            e2e_step(k)
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s_in)
-        for k in range(args.e2e_steps):
-            e2e_step(k)
-        e1.record(s_out)                           # after the last read-back, which follows everything
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, dev)
-    e2e_value = job_rows_per_s(world, rows_per_step, args.e2e_steps, e2e_ms) if args.e2e_steps > 0 else None
-    if int(status.item()) != 0:
-        raise RuntimeError(f"device status {qsa.decode_status(int(status.item()))}")
-
-    if rank == 0:
-        hbm, bf16, bf16_sus, src = peaks()
-        attn_avg = sum(attn_ms) / len(attn_ms)
-        achieved = alg["bytes"] / (attn_avg / 1e3) / 1e9
-        tflops = alg["flops"] / (attn_avg / 1e3) / 1e12
-        t_hbm = alg["bytes"] / (hbm * 1e9) * 1e3
-        t_tc = alg["flops"] / (bf16_sus * 1e12) * 1e3
-        resolved = args.variant or qsa.default_variant()
-        kernel, files = {qsa.ATTN_TCGEN05: ("attn_tc_kernel", ("attn_tc.cu", "tc_ptx.cuh")),
-                         qsa.ATTN_MMA_SYNC: ("attn_mma_kernel", ("attn_mma.cu",)),
-                         qsa.ATTN_TCGEN05_WIDE: ("attn_wide_kernel", ("attn_wide.cu", "tc_ptx.cuh"))}[resolved]
-        srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in files + ("qsa_common.cuh",)]
-        traffic, digest = read_traffic(kernel, srcs)
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(w), "l2": "inputs larger than L2: %.0f MB read + %.0f MB written per step"
-                       % ((sum(v.numel() * v.element_size() for v in d.values())) / 1e6, out.numel() * 4 / 1e6),
-                       "mean_union_cells": round(alg["mean_union"], 1), "union_ratio": round(alg["union_ratio"], 3),
-                       "variant": {1: "tcgen05", 2: "mma.sync", 3: "tcgen05-wide"}[resolved], "parallelism": f"dp{world}"},
-            "roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor", "kernel": kernel,
-                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": traffic, "peak_source": src,
-                         "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
-                         "algorithmic_bytes_per_launch": alg["bytes"], "flops_per_launch": alg["flops"],
-                         "attn_ms": attn_avg, "tflops": tflops, "tensor_frac_sustained": tflops / bf16_sus,
-                         "roofline_ms": max(t_hbm, t_tc), "union_build_ms": sum(union_ms) / len(union_ms),
-                         "source_sha256_16": digest},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": args.e2e_steps,
-                    "pipeline": "copy-in, compute and copy-out streams over two buffer sets"},
-            "gpu_launches": 2 * args.steps,
-            "clocks": clk.summary(),
-        }
-        if world == 1 and not args.no_cpu_baseline:
-            rate, n, dt, cores = oracle_sample(w, args.cpu_seconds)
-            line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                    "sample": f"{n} consecutive query positions x {w.n_heads} heads of the same "
-                                              f"chunk ({dt:.1f} s, FP64, OpenMP)"}
-        print(json.dumps(line), flush=True)
+    if args.context is not None:
+        if args.queries is None:
+            raise SystemExit("a custom chunk needs <context> <queries>")
+        if args.reps is not None:
+            args.steps = int(args.reps)
+        jobs = [(gen.make(custom_config(args, rank)), True)]
+    elif args.all_configs:
+        jobs = [(gen.make(cfg, seed=rank_seed(rank, cfg)), cfg == CONFIG_ID) for cfg in (1, 2, 3, 4, 5)]
+    else:
+        cfg = args.config
+        jobs = [(gen.make(cfg, seed=rank_seed(rank, cfg), n_q=args.n_q), True)]
+    for w, headline in jobs:
+        line = measure(args, w, dev, world, rank, headline)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        del w
+        torch.cuda.empty_cache()
     if world > 1:
         torch.distributed.destroy_process_group()
 

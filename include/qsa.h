@@ -78,9 +78,9 @@ enum {
     QSA_ATTN_DEFAULT = 0,
     QSA_ATTN_TCGEN05 = 1,   /* tcgen05.mma with TMEM accumulators, warp-specialised pipeline,
                                one CTA per (group, KV head), 64-cell chunks, two CTAs per SM */
-    QSA_ATTN_MMA_SYNC = 2,  /* warp-level mma.sync m16n8k16 (legacy tensor path, for comparison) */
-    QSA_ATTN_TCGEN05_WIDE = 3  /* tcgen05, persistent, one CTA per SM over many (group, KV head)
-                                  items, 128-cell chunks, the Q operand in TMEM */
+    QSA_ATTN_TCGEN05_SM = 2 /* tcgen05, one CTA per (group, KV head) and per SM: Q, O and four
+                               S/P buffers in TMEM, two softmax warp sets on alternating chunks
+                               (the kernel qsa_fused_attn runs with the union built in-CTA) */
 };
 
 /* The variant QSA_ATTN_DEFAULT resolves to in this build (one of the values above). */
@@ -94,7 +94,11 @@ const char* qsa_status_str(int status);
  * Returns 0 for n_q < 0 or union_stride <= 0. */
 size_t qsa_union_workspace_bytes(int32_t n_q, int32_t union_stride);
 
-/* Union build (first kernel).  For each group g of up to 8 consecutive queries:
+/* Union build (first kernel).  Defined by "sycl: prompt attention over 8-query
+ * selection unions on XMX" (Strata PR #2808), section Summary (the sorted union of
+ * 8 neighbouring positions' selections, each cell marked by the positions that
+ * chose it) and section Extra Notes (a union cell is an int32 with its 8-position
+ * mask in a separate byte).  For each group g of up to 8 consecutive queries:
  * union_cells[g][0:union_count[g]] = the sorted set union of their selection lists,
  * union_mask[g][u] bit j = query 8g+j selected union_cells[g][u] (bits of absent
  * ragged queries are 0).  Entries past union_count[g] are left unspecified.
@@ -105,15 +109,22 @@ int qsa_union_build(const int32_t* sel, const int32_t* sel_count, int32_t n_q, i
                     int32_t* union_cells, uint8_t* union_mask, int32_t* union_count,
                     int32_t union_stride, int32_t* dev_status, void* stream);
 
-/* Union attention (second kernel).  For query i (group g = i/8, j = i%8) and
- * query head hq: out[i][hq][:] = sum over union cells c with bit j of the mask set
- * and a resident page of softmax(q . k_c * sm_scale) * v_c, with k_c, v_c the
- * dequantised K/V of KV head hq/12; zeros when no such cell exists.  One CTA per
- * (group, KV head) covers 96 rows; K/V chunks of 64 union cells are gathered
- * through the page table and dequantised to BF16 once; the products run on
- * tensor cores with FP32 accumulation.  Typically sm_scale = 1/sqrt(128).
- * Tolerance against an FP64 evaluation: BF16 rounding of Q, K, V and P.
- * `variant` is one of the QSA_ATTN_* values.  n_q == 0 returns QSA_OK. */
+/* Union attention (second kernel).  Defined by "sycl: prompt attention over
+ * 8-query selection unions on XMX" (Strata PR #2808), section Summary: for
+ * query i (group g = i/8, j = i%8) and query head hq, out[i][hq][:] = sum over
+ * union cells c with bit j of the mask set and a resident page of
+ * softmax(q . k_c * sm_scale) * v_c, with k_c, v_c the dequantised K/V of KV
+ * head hq/12; zeros when no such cell exists (our reading for the empty case).
+ * One CTA per (group, KV head) covers 96 rows; K/V chunks of 64 union cells are
+ * gathered through the page table and dequantised once.  Both variants compute
+ * S = Q K^T on FP16 operands (Q converted from BF16, exact, with an exact
+ * power-of-two row scale for rows outside FP16's comfortable range; K as the
+ * exact INT8 integers, its scale applied to the score column in FP32) and
+ * O += P V with FP32 accumulation (QSA_ATTN_TCGEN05: P = p * v_scale rounded to
+ * BF16 against exact BF16 V; QSA_ATTN_TCGEN05_SM: P rounded to FP16 against exact
+ * FP16 V, the V scale carried by a per-chunk power of two).  Typically
+ * sm_scale = 1/sqrt(128).  `variant` is one of the QSA_ATTN_* values.
+ * n_q == 0 returns QSA_OK. */
 int qsa_union_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
                    const uint16_t* k_scale, const uint16_t* v_scale,
                    const int32_t* page_table, int32_t n_lpages, int32_t n_ppages, int32_t n_kv,
@@ -131,6 +142,26 @@ int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
                     float sm_scale, float* out, void* workspace, size_t workspace_bytes,
                     int32_t union_stride, int32_t variant, int32_t* dev_status, void* stream);
+
+/* The whole prompt-attention step in one launch, with each group's union built
+ * inside the attention CTA ("sycl: prompt attention over 8-query selection unions
+ * on XMX", Strata PR #2808, section Summary: the union of 8 neighbouring
+ * positions' sorted selections; section What changed: there the union and the
+ * attention run as a launch pair).  No union arrays reach global memory and no
+ * workspace is needed.  The result is that of qsa_prompt_attn with
+ * variant = QSA_ATTN_TCGEN05_SM, bit for bit: a union-builder warp merges the
+ * group's 8 lists page by page into a shared-memory ring, and the attention
+ * pipeline takes its chunks from there in the same placement.
+ *   - Arguments and layouts are those of qsa_prompt_attn without the workspace,
+ *     union stride and variant.  Lists must be strictly increasing (the union
+ *     build's precondition); counts outside [0, sel_stride] are clamped and
+ *     reported as QSA_DEV_BAD_SEL_COUNT.  Device checks as in qsa_union_attn.
+ *   - n_q == 0 returns QSA_OK with no launch. */
+int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
+                   const uint16_t* k_scale, const uint16_t* v_scale,
+                   const int32_t* page_table, int32_t n_lpages, int32_t n_ppages, int32_t n_kv,
+                   const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
+                   float sm_scale, float* out, int32_t* dev_status, void* stream);
 
 /* Per-position selected-cell attention without unions: out[i][hq][:] is the same
  * softmax over query i's own resident selected cells as qsa_union_attn computes,

@@ -39,7 +39,7 @@ int check_attn_args(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
                     const uint16_t* v_scale, const int32_t* page_table, int32_t n_lpages, int32_t n_ppages,
                     int32_t n_kv, int32_t n_q, float* out, int32_t variant) {
     if (n_q < 0 || n_lpages < 0 || n_ppages < 0 || n_kv <= 0) return QSA_ERR_ARG;
-    if (variant < QSA_ATTN_DEFAULT || variant > QSA_ATTN_TCGEN05_WIDE) return QSA_ERR_ARG;
+    if (variant < QSA_ATTN_DEFAULT || variant > QSA_ATTN_TCGEN05_SM) return QSA_ERR_ARG;
     if (n_q == 0) return QSA_OK;
     if (!q || !out || !page_table) return QSA_ERR_ARG;
     if (n_ppages > 0 && (!k_pool || !v_pool || !k_scale || !v_scale)) return QSA_ERR_ARG;
@@ -99,12 +99,12 @@ int qsa_union_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool
     if (n_q == 0) return QSA_OK;
     if (!union_cells || !union_mask || !union_count) return QSA_ERR_ARG;
     const qsa::AttnArgs a{q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv,
-                          union_cells, union_mask, union_count, union_stride, n_q, sm_scale, out, dev_status};
+                          union_cells, union_mask, union_count, union_stride, n_q, sm_scale, out, dev_status,
+                          nullptr, nullptr, 0};
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (variant == QSA_ATTN_DEFAULT) variant = qsa_attn_default_variant();
-    if (variant == QSA_ATTN_TCGEN05) return cuda_status(qsa::launch_attn_tc(a, s));
-    if (variant == QSA_ATTN_TCGEN05_WIDE) return cuda_status(qsa::launch_attn_wide(a, s));
-    return cuda_status(qsa::launch_attn_mma(a, s));
+    if (variant == QSA_ATTN_TCGEN05_SM) return cuda_status(qsa::launch_attn_sm(a, s));
+    return cuda_status(qsa::launch_attn_tc(a, s));
 }
 
 int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool, const uint16_t* k_scale,
@@ -131,6 +131,22 @@ int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
     if (rc != QSA_OK) return rc;
     return qsa_union_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv, ucell, umask,
                           ucount, union_stride, n_q, sm_scale, out, variant, dev_status, stream);
+}
+
+int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool, const uint16_t* k_scale,
+                   const uint16_t* v_scale, const int32_t* page_table, int32_t n_lpages, int32_t n_ppages,
+                   int32_t n_kv, const int32_t* sel, const int32_t* sel_count, int32_t sel_stride, int32_t n_q,
+                   float sm_scale, float* out, int32_t* dev_status, void* stream) {
+    int rc = check_attn_args(q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv, n_q, out,
+                             QSA_ATTN_DEFAULT);
+    if (rc != QSA_OK) return rc;
+    if (sel_stride <= 0) return QSA_ERR_ARG;
+    if (n_q == 0) return QSA_OK;
+    if (!sel || !sel_count) return QSA_ERR_ARG;
+    const qsa::AttnArgs a{q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv,
+                          nullptr, nullptr, nullptr, 0, n_q, sm_scale, out, dev_status,
+                          sel, sel_count, sel_stride};
+    return cuda_status(qsa::launch_attn_fused(a, static_cast<cudaStream_t>(stream)));
 }
 
 int qsa_select_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool, const uint16_t* k_scale,

@@ -83,6 +83,22 @@ __device__ __forceinline__ void int8x4_to_f16(uint32_t w, uint32_t& out01, uint3
     out23 = f16x2_sub(__byte_perm(u, 0x6464u, 0x5342), 0x64806480u);   // [u2, 0x64, u3, 0x64]
 }
 
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Dequantisation of four INT8 values to FP16 with one FP16 scale s (held in both
+// halves of s2): the exact integers above times s, each product rounded to FP16
+// once (round to nearest even).
+__device__ __forceinline__ void int8x4_to_f16_scaled(uint32_t w, uint32_t s2, uint32_t& out01, uint32_t& out23) {
+    uint32_t a, b;
+    int8x4_to_f16(w, a, b);
+    out01 = f16x2_mul(a, s2);
+    out23 = f16x2_mul(b, s2);
+}
+
 __device__ __forceinline__ void int8x16_to_bf16(uint4 raw, uint4& lo, uint4& hi) {
     int8x4_to_bf16(raw.x, lo.x, lo.y);
     int8x4_to_bf16(raw.y, lo.z, lo.w);
@@ -104,6 +120,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
+// floor(log2 |x|) of a finite, normal, non-zero float (its unbiased exponent field).
+__device__ __forceinline__ int f32_exponent(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
+
+// 2^e exactly, for -126 <= e <= 127.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -115,7 +137,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------- launchers
-// Implemented in union_build.cu / attn_mma.cu / attn_tc.cu; called by capi.cu
+// Implemented in union_build.cu / attn_tc.cu / attn_sm.cu; called by capi.cu
 // after argument validation.  They return cudaGetLastError() of the launch.
 cudaError_t launch_union_build(const int32_t* sel, const int32_t* sel_count, int n_q, int sel_stride,
                                int32_t* union_cells, uint8_t* union_mask, int32_t* union_count,
@@ -136,11 +158,15 @@ struct AttnArgs {
     float sm_scale;
     float* out;
     int32_t* dev_status;
+    // the per-position lists, read by the fused kernel instead of the union arrays
+    const int32_t* sel;
+    const int32_t* sel_count;
+    int sel_stride;
 };
 
-cudaError_t launch_attn_mma(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
-cudaError_t launch_attn_wide(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_sm(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_attn_fused(const AttnArgs& a, cudaStream_t stream);
 
 // Per-position attention (no union): each query over its own selection list,
 // with one shared page table (prompt) or one table per query (decode).

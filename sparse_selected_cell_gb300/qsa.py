@@ -18,7 +18,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libqsa.so")
 
 QSA_OK, QSA_ERR_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CAPACITY, QSA_ERR_CUDA, QSA_ERR_DEVICE_CHECK = range(6)
-ATTN_DEFAULT, ATTN_TCGEN05, ATTN_MMA_SYNC, ATTN_TCGEN05_WIDE = 0, 1, 2, 3
+ATTN_DEFAULT, ATTN_TCGEN05, ATTN_TCGEN05_SM = 0, 1, 2
 DEV_BITS = {1: "bad selection count", 2: "union overflow", 4: "bad cell", 8: "bad page-table entry",
             16: "bad union count", 32: "device wait timeout"}
 
@@ -56,6 +56,8 @@ def lib():
         L.qsa_prompt_attn_static.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _I, _I,
                                              _P, _P]
         L.qsa_prompt_attn_static.restype = ctypes.c_int
+        L.qsa_fused_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
+        L.qsa_fused_attn.restype = ctypes.c_int
         L.qsa_select_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
         L.qsa_select_attn.restype = ctypes.c_int
         L.qsa_decode_attn.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _I, _I, _F, _P, _P, _P]
@@ -88,6 +90,26 @@ def _dev(t: torch.Tensor, name: str, dtypes) -> torch.Tensor:
 
 _B16 = (torch.bfloat16, torch.int16, torch.uint16)
 _H16 = (torch.float16, torch.int16, torch.uint16)
+
+
+def _attn_inputs(q, k_pool, v_pool, k_scale, v_scale, page_table, out):
+    """Device, dtype and shape checks shared by the attention calls; returns out
+    (allocated here when not given: float32 [n_q, n_kv*12, 128])."""
+    _dev(q, "q", _B16)
+    _dev(k_pool, "k_pool", (torch.int8,))
+    _dev(v_pool, "v_pool", (torch.int8,))
+    _dev(k_scale, "k_scale", _H16)
+    _dev(v_scale, "v_scale", _H16)
+    _dev(page_table, "page_table", (torch.int32,))
+    if q.dim() != 3 or q.shape[2] != gen.HEAD_DIM or q.shape[1] % gen.HEADS_PER_KV != 0:
+        raise ValueError(f"q must be [n_q, n_kv*12, 128], got {tuple(q.shape)}")
+    shape = (int(q.shape[0]), int(q.shape[1]), gen.HEAD_DIM)
+    if out is None:
+        return torch.empty(shape, dtype=torch.float32, device=q.device)
+    _dev(out, "out", (torch.float32,))
+    if tuple(out.shape) != shape:
+        raise ValueError(f"out must have shape {shape}, got {tuple(out.shape)}")
+    return out
 
 
 def _check(fn: str, rc: int):
@@ -126,17 +148,9 @@ def union_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, union_cells, uni
                sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None, variant: int = ATTN_DEFAULT,
                dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Union attention -> out float32 [n_q, n_kv*12, 128]."""
-    _dev(q, "q", _B16)
-    _dev(k_pool, "k_pool", (torch.int8,))
-    _dev(v_pool, "v_pool", (torch.int8,))
-    _dev(k_scale, "k_scale", _H16)
-    _dev(v_scale, "v_scale", _H16)
-    _dev(page_table, "page_table", (torch.int32,))
+    out = _attn_inputs(q, k_pool, v_pool, k_scale, v_scale, page_table, out)
     n_q, n_heads = int(q.shape[0]), int(q.shape[1])
     n_kv = n_heads // gen.HEADS_PER_KV
-    if out is None:
-        out = torch.empty((n_q, n_heads, gen.HEAD_DIM), dtype=torch.float32, device=q.device)
-    _dev(out, "out", (torch.float32,))
     if sm_scale is None:
         sm_scale = gen.HEAD_DIM ** -0.5
     rc = lib().qsa_union_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
@@ -152,6 +166,7 @@ def prompt_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
                 workspace: Optional[torch.Tensor] = None, union_stride: int = gen.UNION_STRIDE,
                 variant: int = ATTN_DEFAULT, dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Union build + union attention in one call, over a caller-owned workspace."""
+    out = _attn_inputs(q, k_pool, v_pool, k_scale, v_scale, page_table, out)
     _dev(sel, "sel", (torch.int32,))
     _dev(sel_count, "sel_count", (torch.int32,))
     n_q, n_heads = int(q.shape[0]), int(q.shape[1])
@@ -159,8 +174,6 @@ def prompt_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
     need = workspace_bytes(n_q, union_stride)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    if out is None:
-        out = torch.empty((n_q, n_heads, gen.HEAD_DIM), dtype=torch.float32, device=q.device)
     if sm_scale is None:
         sm_scale = gen.HEAD_DIM ** -0.5
     rc = lib().qsa_prompt_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
@@ -172,23 +185,34 @@ def prompt_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
     return out
 
 
-def select_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
-                sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Per-position attention without unions (qsa_select_attn) -> out float32 [n_q, n_kv*12, 128]."""
-    _dev(q, "q", _B16)
-    _dev(k_pool, "k_pool", (torch.int8,))
-    _dev(v_pool, "v_pool", (torch.int8,))
-    _dev(k_scale, "k_scale", _H16)
-    _dev(v_scale, "v_scale", _H16)
-    _dev(page_table, "page_table", (torch.int32,))
+def fused_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
+               sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+               dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """qsa_fused_attn: the prompt-attention step in one launch, each group's union
+    built inside the attention CTA (no workspace) -> out float32 [n_q, n_kv*12, 128]."""
+    out = _attn_inputs(q, k_pool, v_pool, k_scale, v_scale, page_table, out)
     _dev(sel, "sel", (torch.int32,))
     _dev(sel_count, "sel_count", (torch.int32,))
     n_q, n_heads = int(q.shape[0]), int(q.shape[1])
     n_kv = n_heads // gen.HEADS_PER_KV
-    if out is None:
-        out = torch.empty((n_q, n_heads, gen.HEAD_DIM), dtype=torch.float32, device=q.device)
-    _dev(out, "out", (torch.float32,))
+    if sm_scale is None:
+        sm_scale = gen.HEAD_DIM ** -0.5
+    rc = lib().qsa_fused_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
+                              int(page_table.shape[0]), int(k_pool.shape[0]), n_kv, _ptr(sel), _ptr(sel_count),
+                              int(sel.shape[1]), n_q, float(sm_scale), _ptr(out), _ptr(dev_status), _stream(stream))
+    _check("qsa_fused_attn", rc)
+    return out
+
+
+def select_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel_count,
+                sm_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                dev_status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Per-position attention without unions (qsa_select_attn) -> out float32 [n_q, n_kv*12, 128]."""
+    out = _attn_inputs(q, k_pool, v_pool, k_scale, v_scale, page_table, out)
+    _dev(sel, "sel", (torch.int32,))
+    _dev(sel_count, "sel_count", (torch.int32,))
+    n_q, n_heads = int(q.shape[0]), int(q.shape[1])
+    n_kv = n_heads // gen.HEADS_PER_KV
     if sm_scale is None:
         sm_scale = gen.HEAD_DIM ** -0.5
     rc = lib().qsa_select_attn(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale), _ptr(page_table),
@@ -248,12 +272,11 @@ def prompt_attn_static(q, k_pool, v_pool, k_scale, v_scale, page_table, sel, sel
     """qsa_prompt_attn_static: the prompt-attention step over the library's static
     device scratch (no workspace, no allocation inside the call).  Only `out`, when
     not given, is allocated here, by the caller's side of the binding."""
+    out = _attn_inputs(q, k_pool, v_pool, k_scale, v_scale, page_table, out)
     _dev(sel, "sel", (torch.int32,))
     _dev(sel_count, "sel_count", (torch.int32,))
     n_q, n_heads = int(q.shape[0]), int(q.shape[1])
     n_kv = n_heads // gen.HEADS_PER_KV
-    if out is None:
-        out = torch.empty((n_q, n_heads, gen.HEAD_DIM), dtype=torch.float32, device=q.device)
     if sm_scale is None:
         sm_scale = gen.HEAD_DIM ** -0.5
     rc = lib().qsa_prompt_attn_static(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(k_scale), _ptr(v_scale),

@@ -67,6 +67,7 @@ def test_host_argument_checks(lib):
     assert _attn(lib) == ERR_ARG
     assert _attn(lib, n_kv=0) == ERR_ARG
     assert _attn(lib, variant=7) == ERR_ARG
+    assert _attn(lib, variant=3) == ERR_ARG   # no such variant (QSA_ATTN_TCGEN05_SM is the last)
     # misaligned q / out pointers (never dereferenced: rejected on the host)
     fake = ctypes.c_void_p(0x1000)
     odd = ctypes.c_void_p(0x1008)
@@ -93,3 +94,19 @@ def test_decode_host_argument_checks(lib):
     assert dec(-1) == ERR_ARG                 # negative page-table stride
     assert dec(3) == ERR_ARG                  # tables would overlap: 0 < pt_stride < n_lpages
     assert dec(4, sel_stride=0) == ERR_ARG
+
+
+def test_fused_host_argument_checks(lib):
+    ERR_ARG = 1
+    fake = ctypes.c_void_p(0x100000)
+    f = ctypes.c_float(0.088)
+
+    def fused(n_q=8, sel_stride=2056, sel=fake, cnt=fake, n_kv=1):
+        return lib.qsa_fused_attn(fake, fake, fake, fake, fake, fake, 4, 16, n_kv, sel, cnt, sel_stride, n_q, f, fake,
+                                  None, None)
+    assert fused(n_q=0) == 0                  # nothing to do, no launch
+    assert fused(n_q=-1) == ERR_ARG
+    assert fused(sel_stride=0) == ERR_ARG
+    assert fused(sel=None) == ERR_ARG
+    assert fused(cnt=None) == ERR_ARG
+    assert fused(n_kv=0) == ERR_ARG

@@ -15,7 +15,7 @@ from sparse_selected_cell_gb300 import gen
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [1, 2, 3]   # QSA_ATTN_TCGEN05, QSA_ATTN_MMA_SYNC, QSA_ATTN_TCGEN05_WIDE
+VARIANTS = [1, 2]   # QSA_ATTN_TCGEN05 (two CTAs per SM, the default), QSA_ATTN_TCGEN05_SM (one CTA per SM)
 
 
 @pytest.fixture(scope="module")
