@@ -12,9 +12,13 @@
 // over a batch of sequences (qsa_decode_attn): query i is sequence i's current
 // position, with its own page table at page_table + i * pt_stride.
 //
-// One warp per (query position i, KV head h): its 12 query heads are rows 0-11
-// of one m16 tile (rows 12-15 padding), Q held as A fragments in registers.  The
-// position's list is walked in steps of 16 cells:
+// One warp per (query position i, KV head h) -- or, for decode, one CTA per
+// (query, KV head) whose 4 warps each take a quarter of the list and merge their
+// partial softmax states at the end (flash-decoding style: decode batches have
+// few (query, KV head) items, and four times as many CTAs fill the GPU in many
+// waves instead of 2.25).  A warp's 12 query heads are rows 0-11 of one m16 tile
+// (rows 12-15 padding), Q held as A fragments in registers.  The warp's part of
+// the list is walked in steps of 16 cells:
 //   * lanes 0-15 resolve cell -> page -> pool row for the K rows, lanes 16-31 for
 //     the V rows, in a three-step register pipeline (cells two steps ahead, the
 //     page table one step ahead), and issue 16-byte cp.async copies of the rows
@@ -81,19 +85,26 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpSmem& s = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
-    const long long item = (long long)blockIdx.x * kSelWarps + warp;   // h-major: consecutive positions share cells
-    if (item >= (long long)a.n_q * a.n_kv) return;
+    const bool split = a.split4 != 0;
+    // h-major: consecutive positions share cells
+    const long long item = split ? (long long)blockIdx.x : (long long)blockIdx.x * kSelWarps + warp;
+    if (item >= (long long)a.n_q * a.n_kv) return;   // (a split CTA's warps share one item: all or none leave)
     const int h = (int)(item / a.n_q), i = (int)(item - (long long)h * a.n_q);
     const int n_heads = a.n_kv * kHeadsPerKv;
     const float kmul = a.sm_scale * kLog2e;
 
     int cnt = __ldg(a.sel_count + i);
     if (cnt < 0 || cnt > a.sel_stride) {
-        if (lane == 0) report(a.dev_status, QSA_DEV_BAD_SEL_COUNT);
+        if (lane == 0 && (!split || warp == 0)) report(a.dev_status, QSA_DEV_BAD_SEL_COUNT);
         cnt = cnt < 0 ? 0 : a.sel_stride;
     }
-    const int n_steps = (cnt + kStep - 1) / kStep;
-    const int32_t* lst = a.sel + (size_t)i * a.sel_stride;
+    // this warp's part of the list: whole 16-cell steps [first, first + n_steps)
+    const int all_steps = (cnt + kStep - 1) / kStep;
+    const int per_warp = split ? (all_steps + kSelWarps - 1) / kSelWarps : all_steps;
+    const int first = split ? min(all_steps, warp * per_warp) : 0;
+    const int n_steps = min(all_steps, first + per_warp) - first;
+    const int32_t* lst = a.sel + (size_t)i * a.sel_stride + first * kStep;
+    cnt -= first * kStep;
     const int32_t* ptab = a.page_table + (size_t)i * a.pt_stride;   // this query's page table
 
     // ---- cell -> page -> row pipeline: lane l handles cell (l & 15) of a step, K (l < 16) or V (l >= 16)
@@ -287,9 +298,56 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
     float* out0 = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + r0) * kHeadDim;
     float* out1 = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + (v1 ? r1 : 0)) * kHeadDim;
+    if (split) {
+        // Merge the four warps' partial states.  Warp w's O and l are relative to
+        // its own running max m_w; the row's result is sum_w 2^(m_w - M) O_w over
+        // sum_w 2^(m_w - M) l_w with M = max_w m_w (a warp with no valid cell has
+        // m_w = -inf and weight 0).  The stage buffers are free now.
+        __syncthreads();
+        float* po = reinterpret_cast<float*>(smem_raw);                  // [warp][16 rows][128]
+        float* pm = po + kSelWarps * 16 * kHeadDim;                      // [warp][16 rows]
+        float* pl = pm + kSelWarps * 16;                                 // [warp][16 rows]
+#pragma unroll
+        for (int dt = 0; dt < 16; ++dt) {
+            const int d = dt * 8 + 2 * t4;
+            *reinterpret_cast<float2*>(po + (warp * 16 + r0) * kHeadDim + d) = make_float2(o[dt][0], o[dt][1]);
+            *reinterpret_cast<float2*>(po + (warp * 16 + r1) * kHeadDim + d) = make_float2(o[dt][2], o[dt][3]);
+        }
+        if (t4 == 0) {
+            pm[warp * 16 + r0] = m0;
+            pm[warp * 16 + r1] = m1;
+            pl[warp * 16 + r0] = l0;
+            pl[warp * 16 + r1] = l1;
+        }
+        __syncthreads();
+        // thread t: rows 0-11, 4 consecutive dims each step
+        for (int e = threadIdx.x; e < kHeadsPerKv * (kHeadDim / 4); e += kSelThreads) {
+            const int row = e / (kHeadDim / 4), d = 4 * (e - row * (kHeadDim / 4));
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kSelWarps; ++w) M = fmaxf(M, pm[w * 16 + row]);
+            float L = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kSelWarps; ++w) {
+                const float mw = pm[w * 16 + row];
+                const float wt = mw == -INFINITY ? 0.f : fast_exp2(mw - M);
+                L += wt * pl[w * 16 + row];
+                const float4 ow = *reinterpret_cast<const float4*>(po + (w * 16 + row) * kHeadDim + d);
+                acc.x += wt * ow.x;
+                acc.y += wt * ow.y;
+                acc.z += wt * ow.z;
+                acc.w += wt * ow.w;
+            }
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            float* dst = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + row) * kHeadDim + d;
+            *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        }
+        return;
+    }
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int dt = 0; dt < 16; ++dt) {
         const int d = dt * 8 + 2 * t4;
@@ -305,7 +363,7 @@ cudaError_t launch_select_attn(const SelArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(select_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long items = (long long)a.n_q * a.n_kv;
-    const unsigned grid = (unsigned)((items + kSelWarps - 1) / kSelWarps);
+    const unsigned grid = a.split4 ? (unsigned)items : (unsigned)((items + kSelWarps - 1) / kSelWarps);
     select_attn_kernel<<<grid, kSelThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
