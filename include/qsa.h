@@ -229,13 +229,19 @@ int qsa_wait_selftest(int32_t limit_us, int32_t* dev_status, void* stream);
  * in this library's static device memory (one per device), and the result is
  * that of qsa_prompt_attn on a workspace of that size.
  *   - Arguments, layouts and ownership are those of qsa_prompt_attn; the
- *     stream must belong to the current device.
- *   - Returns QSA_ERR_CAPACITY, before any CUDA call, when
- *     qsa_union_workspace_bytes(n_q, union_stride) > QSA_STATIC_SCRATCH_BYTES;
- *     QSA_ERR_CUDA when the scratch's address cannot be resolved.
+ *     stream must belong to the current device (QSA_ERR_ARG otherwise).
+ *   - Checks that need no CUDA call come first, in this order: sizes, shape
+ *     arguments and variant (QSA_ERR_ARG), then capacity: QSA_ERR_CAPACITY when
+ *     qsa_union_workspace_bytes(n_q, union_stride) > QSA_STATIC_SCRATCH_BYTES,
+ *     then null pointers (QSA_ERR_ARG).  QSA_ERR_CUDA when the scratch's
+ *     address cannot be resolved.
  *   - The first call on each device resolves the scratch's address with
  *     cudaGetSymbolAddress (this may load the library's device code on that
- *     device); make that first call before any stream capture begins.
+ *     device) and caches it for the life of the process; make that first call
+ *     before any stream capture begins.  The cached address is not valid after
+ *     cudaDeviceReset (the module is loaded again and the scratch may move):
+ *     a process that resets a device must not call this entry point on that
+ *     device afterwards.
  *   - Nothing in the scratch must start at zero (the union build writes all
  *     that the attention kernel reads), so no call clears it.
  *   - All calls on one device share the one scratch: two calls whose work can

@@ -757,10 +757,6 @@ __device__ __forceinline__ void scale_mask16(uint32_t* s, uint32_t sel, bool uni
     }
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    const __half2 v = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // Weights e = 2^(x - m) for 16 columns: e is added to la / lb (the row's sum),
 // and e * vs (vs: the 16 columns' scaled V scales in shared memory) goes out as

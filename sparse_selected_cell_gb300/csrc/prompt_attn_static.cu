@@ -60,14 +60,24 @@ extern "C" int qsa_prompt_attn_static(const uint16_t* q, const int8_t* k_pool, c
                                       const int32_t* sel_count, int32_t sel_stride, int32_t n_q, float sm_scale,
                                       float* out, int32_t union_stride, int32_t variant, int32_t* dev_status,
                                       void* stream) {
-    // size checks first, before anything touches CUDA
+    // host-only checks first, before anything touches CUDA: sizes and shape
+    // arguments, then the scratch's capacity, then the pointers
     if (n_q < 0 || union_stride <= 0 || union_stride % 64 != 0) return QSA_ERR_ARG;
+    if (n_lpages < 0 || n_ppages < 0 || n_kv <= 0 || sel_stride <= 0) return QSA_ERR_ARG;
+    if (variant < QSA_ATTN_DEFAULT || variant > QSA_ATTN_TCGEN05_SM) return QSA_ERR_ARG;
     if (n_q == 0)
         return qsa_prompt_attn(q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv, sel,
                                sel_count, sel_stride, n_q, sm_scale, out, nullptr, 0, union_stride, variant,
                                dev_status, stream);
     if (qsa_union_workspace_bytes(n_q, union_stride) > (size_t)QSA_STATIC_SCRATCH_BYTES) return QSA_ERR_CAPACITY;
     if (!q || !out || !page_table || !sel || !sel_count) return QSA_ERR_ARG;
+    // the scratch used is the current device's: a stream of another device is refused
+    if (stream != nullptr) {
+        int dev = -1, sdev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
+        if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev) != cudaSuccess) return QSA_ERR_ARG;
+        if (sdev != dev) return QSA_ERR_ARG;
+    }
     void* scratch = nullptr;
     const int rc = scratch_on_current_device(&scratch);
     if (rc != QSA_OK) return rc;
