@@ -160,7 +160,7 @@ int qsa_select_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
     if (n_q == 0) return QSA_OK;
     if (!sel || !sel_count) return QSA_ERR_ARG;
     const qsa::SelArgs a{q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv,
-                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status, 0, 0};
+                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status, 0};
     return cuda_status(qsa::launch_select_attn(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -175,7 +175,7 @@ int qsa_decode_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
     if (n_q == 0) return QSA_OK;
     if (!sel || !sel_count) return QSA_ERR_ARG;
     const qsa::SelArgs a{q, k_pool, v_pool, k_scale, v_scale, page_tables, n_lpages, n_ppages, n_kv,
-                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status, pt_stride, 1};
+                         sel, sel_count, sel_stride, n_q, sm_scale, out, dev_status, pt_stride};
     return cuda_status(qsa::launch_select_attn(a, static_cast<cudaStream_t>(stream)));
 }
 

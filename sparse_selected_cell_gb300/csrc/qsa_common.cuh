@@ -190,7 +190,6 @@ struct SelArgs {
     float* out;
     int32_t* dev_status;
     int pt_stride;
-    int split4;                  // 1: one CTA per (query, KV head), its 4 warps split the list
 };
 
 cudaError_t launch_select_attn(const SelArgs& a, cudaStream_t stream);

@@ -12,23 +12,27 @@
 // over a batch of sequences (qsa_decode_attn): query i is sequence i's current
 // position, with its own page table at page_table + i * pt_stride.
 //
-// One warp per (query position i, KV head h) -- or, for decode, one CTA per
-// (query, KV head) whose 4 warps each take a quarter of the list and merge their
-// partial softmax states at the end (flash-decoding style: decode batches have
-// few (query, KV head) items, and four times as many CTAs fill the GPU in many
-// waves instead of 2.25).  A warp's 12 query heads are rows 0-11 of one m16 tile
-// (rows 12-15 padding), Q held as A fragments in registers.  The warp's part of
-// the list is walked in steps of 16 cells:
+// One CTA of four warps per (query position i, KV head h): the warps each take a
+// quarter of the position's list and merge their partial softmax states at the
+// end (flash-decoding style: decode batches have few (query, KV head) items,
+// and four CTAs' worth of warps per item fill the GPU in many waves).  The 12
+// query heads are rows 0-11 of one m16 tile (rows 12-15 padding); the CTA keeps
+// Q once in shared memory, and each warp reads its A fragments with ldmatrix.
+// A warp walks its part of the list in steps of 16 cells:
 //   * lanes 0-15 resolve cell -> page -> pool row for the K rows, lanes 16-31 for
-//     the V rows, in a three-step register pipeline (cells two steps ahead, the
-//     page table one step ahead), and issue 16-byte cp.async copies of the rows
-//     into a 3-deep INT8 stage ring, two steps ahead of the step being
-//     computed (16-byte chunks XOR-swizzled by cell);
-//   * the warp converts the stage exactly to BF16 tiles (|int8| <= 127 fits
-//     BF16), S = Q K^T with mma.sync m16n8k16, the K scale (times sm_scale and
-//     log2 e) multiplies each score column in FP32, unselected / masked cells
-//     are -inf, the online softmax runs in the exp2 domain with the same lazy
-//     rescale as the union kernel, P = p * (V scale) enters O += P V as BF16.
+//     the V rows, in a register pipeline (while step t is computed: the cells
+//     of step t+3 and the page-table entries of step t+2 are loaded, and step
+//     t+1's rows are copied with 16-byte cp.async into a 2-deep INT8 stage
+//     ring, 16-byte chunks XOR-swizzled by cell); the rows' K/V scales are
+//     loaded with the copies and stored a step later, so no step waits on them;
+//   * S = Q K^T with mma.sync m16n8k16 on BF16 operands: each lane's K operand
+//     is one 32-bit word of the INT8 row (the head dimension is permuted inside
+//     every 16-wide k step, for Q and K alike), converted exactly in registers
+//     (|int8| <= 127 fits BF16); the K scale (times sm_scale and log2 e)
+//     multiplies each score column in FP32, unselected / masked cells are -inf,
+//     the online softmax runs in the exp2 domain with the same lazy rescale as
+//     the union kernel, and P = p * (V scale) enters O += P V as BF16, with V
+//     converted exactly to a BF16 tile read by ldmatrix.trans.
 #include "qsa_common.cuh"
 
 namespace qsa {
@@ -37,8 +41,15 @@ namespace {
 constexpr int kSelWarps = 4;
 constexpr int kSelThreads = 32 * kSelWarps;
 constexpr int kStep = 16;                  // cells per step
-constexpr int kStages = 3;                 // INT8 stage ring: copies run kStages - 1 steps ahead
+constexpr int kStages = 2;                 // INT8 stage ring: copies run kStages - 1 steps ahead
 constexpr float kSelRescaleLog2 = 32.f;    // lazy rescale threshold (exp2 domain), as in attn_tc.cu
+
+// The (query, KV head)'s 12 query-head rows as FP16 (rows 12-15 zero), shared by
+// the CTA's four warps: 256-byte rows, 16-byte chunks XOR-swizzled by (row & 7),
+// each 16-wide k step in the permuted order the S fragments use (see below).
+struct __align__(16) QTile {
+    uint16_t q[16][kHeadDim];
+};
 
 struct __align__(16) WarpSmem {
     int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   12 KB
@@ -85,23 +96,23 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpSmem& s = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
-    const bool split = a.split4 != 0;
+    QTile& qt = *reinterpret_cast<QTile*>(smem_raw + kSelWarps * sizeof(WarpSmem));
     // h-major: consecutive positions share cells
-    const long long item = split ? (long long)blockIdx.x : (long long)blockIdx.x * kSelWarps + warp;
-    if (item >= (long long)a.n_q * a.n_kv) return;   // (a split CTA's warps share one item: all or none leave)
+    const long long item = (long long)blockIdx.x;
+    if (item >= (long long)a.n_q * a.n_kv) return;   // the CTA's warps share one item: all or none leave
     const int h = (int)(item / a.n_q), i = (int)(item - (long long)h * a.n_q);
     const int n_heads = a.n_kv * kHeadsPerKv;
     const float kmul = a.sm_scale * kLog2e;
 
     int cnt = __ldg(a.sel_count + i);
     if (cnt < 0 || cnt > a.sel_stride) {
-        if (lane == 0 && (!split || warp == 0)) report(a.dev_status, QSA_DEV_BAD_SEL_COUNT);
+        if (lane == 0 && warp == 0) report(a.dev_status, QSA_DEV_BAD_SEL_COUNT);
         cnt = cnt < 0 ? 0 : a.sel_stride;
     }
     // this warp's part of the list: whole 16-cell steps [first, first + n_steps)
     const int all_steps = (cnt + kStep - 1) / kStep;
-    const int per_warp = split ? (all_steps + kSelWarps - 1) / kSelWarps : all_steps;
-    const int first = split ? min(all_steps, warp * per_warp) : 0;
+    const int per_warp = (all_steps + kSelWarps - 1) / kSelWarps;
+    const int first = min(all_steps, warp * per_warp);
     const int n_steps = min(all_steps, first + per_warp) - first;
     const int32_t* lst = a.sel + (size_t)i * a.sel_stride + first * kStep;
     cnt -= first * kStep;
@@ -126,8 +137,11 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         }
         return pp;
     };
-    auto issue = [&](int cell, int page, int st) {
-        float sc = 0.f;
+    // Row copies of a step into stage st, and the load of the lane's scale (its
+    // FP16 bits, 0 for a masked cell), which put_scale stores one step later, so
+    // the load's latency is not waited for in the step that issues it.
+    auto issue = [&](int cell, int page, int st) -> uint16_t {
+        uint16_t sb = 0;
         const bool ok = page >= 0;
         if (ok) {
             const size_t row = ((size_t)page * a.n_kv + h) * kPage + (cell & (kPage - 1));
@@ -135,40 +149,64 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
             const uint32_t dst = smem_u32(&s.raw[st][kv][slot][0]);
 #pragma unroll
             for (int seg = 0; seg < 8; ++seg) cp_async16(dst + ((seg ^ (slot & 7)) << 4), src + seg * 16);
-            sc = __half2float(__ushort_as_half(__ldg((kv ? a.v_scale : a.k_scale) + row)));
+            sb = __ldg((kv ? a.v_scale : a.k_scale) + row);
         }
-        if (kv) s.vs[st][slot] = ok ? sc : 0.f;
-        else s.ks[st][slot] = ok ? sc * kmul : 0.f;
         const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
         if (lane == 0) s.valid[st] = vm;
+        return sb;
+    };
+    // A masked cell's scale is 0 (its score is -inf anyway; P is 0).
+    auto put_scale = [&](uint16_t sb, int st) {
+        const float sc = __half2float(__ushort_as_half(sb));
+        if (kv) s.vs[st][slot] = sc;
+        else s.ks[st][slot] = sc * kmul;
     };
 
-    // prologue: copies of steps 0 .. kStages-2 in flight; then the register
-    // pipeline holds the cells of step kStages-1 (resolved) and kStages
+    // prologue: copies of steps 0 .. kStages-2 in flight (their scales stored
+    // now); then the register pipeline holds the cells of step kStages-1
+    // (resolved) and kStages
 #pragma unroll 1
     for (int k = 0; k < kStages - 1; ++k) {
         const int c = load_cell(k);
-        issue(c, resolve(c), k);
+        put_scale(issue(c, resolve(c), k), k);
         cp_async_commit();
     }
     int c1 = load_cell(kStages - 1), c2 = load_cell(kStages);
     int p1 = resolve(c1);
+    uint16_t sb_next = 0;   // scale of step + kStages - 2 (loaded one step ago), stored at the next step's top
 
-    // ---- Q fragments (A operand): rows 0-11 are the KV head's 12 query heads
+    // ---- Q (A operand of S, BF16), rows 0-11: the KV head's 12 query heads.  The
+    // head dimension is permuted inside each 16-wide k step, for Q and K alike (a
+    // dot product does not depend on the order of its terms): logical entries
+    // 2t, 2t+1, 2t+8, 2t+9 of a k step -- what lane (g, t) holds of an m16n8k16
+    // fragment -- are dims 16kk + 4t .. 16kk + 4t + 3, so a lane's K operand is
+    // one 32-bit word of the INT8 row.  Thread t of the CTA stores row t >> 3,
+    // k step t & 7 (16 dims).
+    {
+        const int row = threadIdx.x >> 3, kk = threadIdx.x & 7;
+        const bool live = row < kHeadsPerKv;
+        const uint4* src = reinterpret_cast<const uint4*>(
+            a.q + ((size_t)i * n_heads + h * kHeadsPerKv + (live ? row : 0)) * kHeadDim + 16 * kk);
+        uint4 x[2] = {live ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u), live ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u)};
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(x);
+        // logical position j of physical dim p = 4t + 2hi + b (b, hi in {0, 1}): j = 2t + b + 8hi
+        uint32_t lg[8];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            lg[t] = w[2 * t];            // dims 4t, 4t+1
+            lg[4 + t] = w[2 * t + 1];    // dims 4t+2, 4t+3
+        }
+        uint8_t* qrow = reinterpret_cast<uint8_t*>(&qt.q[row][0]);
+        *reinterpret_cast<uint4*>(qrow + (((2 * kk) ^ (row & 7)) << 4)) = make_uint4(lg[0], lg[1], lg[2], lg[3]);
+        *reinterpret_cast<uint4*>(qrow + (((2 * kk + 1) ^ (row & 7)) << 4)) = make_uint4(lg[4], lg[5], lg[6], lg[7]);
+    }
+    __syncthreads();
     const int g4 = lane >> 2, t4 = lane & 3;
     const int r0 = g4, r1 = g4 + 8;
-    const bool v1 = r1 < kHeadsPerKv;
-    const uint16_t* q0p = a.q + ((size_t)i * n_heads + h * kHeadsPerKv + r0) * kHeadDim;
-    const uint16_t* q1p = a.q + ((size_t)i * n_heads + h * kHeadsPerKv + (v1 ? r1 : 0)) * kHeadDim;
-    uint32_t qa[8][4];
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-        const int d = kk * 16 + 2 * t4;
-        qa[kk][0] = __ldg(reinterpret_cast<const uint32_t*>(q0p + d));
-        qa[kk][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1p + d)) : 0u;
-        qa[kk][2] = __ldg(reinterpret_cast<const uint32_t*>(q0p + d + 8));
-        qa[kk][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(q1p + d + 8)) : 0u;
-    }
+    // ldmatrix x4 row addresses of the Q tile: lane l reads row (l & 7) + 8 ((l >> 3) & 1),
+    // logical chunk 2 kk + (l >> 4)
+    const int qr = (lane & 7) + 8 * ((lane >> 3) & 1);
+    const uint32_t q_base = smem_u32(&qt.q[qr][0]);
 
     float o[16][4];
 #pragma unroll
@@ -183,17 +221,19 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         // step+kStages-1 (into the stage step-1 used), while step's copies land
         const int c3 = load_cell(step + kStages + 1);
         const int p2 = resolve(c2);
-        issue(c1, p1, (step + kStages - 1) % kStages);
+        // scales of step + kStages - 2 (its copies were issued one step ago; step 1's
+        // were stored in the prologue), then step + kStages - 1's copies and scale load
+        if (step > 0) put_scale(sb_next, (step + kStages - 2) % kStages);
+        sb_next = issue(c1, p1, (step + kStages - 1) % kStages);
         cp_async_commit();
         cp_async_wait<kStages - 1>();
         __syncwarp();
 
-        // exact BF16 tile (K first, then V in the same space): lane l converts 64
-        // bytes (half l & 1) of cell (l >> 1)
-        auto convert = [&](int tv) {
+        // exact BF16 V tile: lane l converts 64 bytes (half l & 1) of cell (l >> 1)
+        {
             const int cell = lane >> 1, hh = lane & 1;
             uint8_t* dst = reinterpret_cast<uint8_t*>(&s.kb[0][0]);
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(&s.raw[st][tv][cell][0]);
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(&s.raw[st][1][cell][0]);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int seg = 4 * hh + k;
@@ -203,26 +243,31 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
                 *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg, 256)) = lo;
                 *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg + 1, 256)) = hi;
             }
-        };
-        convert(0);
-        __syncwarp();
+        }
 
-        // S = Q K^T: 16 rows x 16 cells
+        // S = Q K^T: 16 rows x 16 cells, K straight from the INT8 stage: lane (g, t)
+        // of n tile nt reads dims 16kk + 4t .. +3 of cell 8nt + g (one 32-bit word;
+        // the stage's 16-byte chunks are XOR-swizzled by cell, so the 32 lanes hit
+        // 32 different banks) and converts them exactly to two FP16 pairs.  Even and
+        // odd k steps accumulate separately (two shorter dependency chains).
         float sc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-            const int cell = nt * 8 + (lane & 7);
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            const int cell = nt * 8 + g4;
+            const uint8_t* krow = reinterpret_cast<const uint8_t*>(&s.raw[st][0][cell][0]) + 4 * t4;
 #pragma unroll
-            for (int kk2 = 0; kk2 < 4; ++kk2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb_base + swz(cell, 4 * kk2 + (lane >> 3), 256), b0, b1, b2, b3);
-                mma_bf16(sc[nt], qa[2 * kk2], b0, b1);
-                mma_bf16(sc[nt], qa[2 * kk2 + 1], b2, b3);
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t qa[4];
+                ldsm_x4(q_base + (((2 * kk + (lane >> 4)) ^ (qr & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(krow + ((kk ^ (cell & 7)) << 4));
+                uint32_t b0, b1;
+                int8x4_to_bf16(w, b0, b1);
+                mma_bf16(acc[kk & 1], qa, b0, b1);
             }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) sc[nt][v] = acc[0][v] + acc[1][v];
         }
-        __syncwarp();   // every lane has read K out of the tile
-        convert(1);     // V into the same tile (read after the softmax below)
         // column scale (log2 domain), masked cells -inf
         const uint32_t vm = s.valid[st];
         float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -298,9 +343,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
     l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
     l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    float* out0 = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + r0) * kHeadDim;
-    float* out1 = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + (v1 ? r1 : 0)) * kHeadDim;
-    if (split) {
+    {
         // Merge the four warps' partial states.  Warp w's O and l are relative to
         // its own running max m_w; the row's result is sum_w 2^(m_w - M) O_w over
         // sum_w 2^(m_w - M) l_w with M = max_w m_w (a warp with no valid cell has
@@ -345,25 +388,17 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
             float* dst = a.out + ((size_t)i * n_heads + h * kHeadsPerKv + row) * kHeadDim + d;
             *reinterpret_cast<float4*>(dst) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         }
-        return;
-    }
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-#pragma unroll
-    for (int dt = 0; dt < 16; ++dt) {
-        const int d = dt * 8 + 2 * t4;
-        *reinterpret_cast<float2*>(out0 + d) = make_float2(o[dt][0] * inv0, o[dt][1] * inv0);
-        if (v1) *reinterpret_cast<float2*>(out1 + d) = make_float2(o[dt][2] * inv1, o[dt][3] * inv1);
     }
 }
 
 }  // namespace
 
 cudaError_t launch_select_attn(const SelArgs& a, cudaStream_t stream) {
-    const int smem = (int)(kSelWarps * sizeof(WarpSmem));
+    const int smem = (int)(kSelWarps * sizeof(WarpSmem) + sizeof(QTile));
     cudaError_t e = cudaFuncSetAttribute(select_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const long long items = (long long)a.n_q * a.n_kv;
-    const unsigned grid = a.split4 ? (unsigned)items : (unsigned)((items + kSelWarps - 1) / kSelWarps);
+    const unsigned grid = (unsigned)items;
     select_attn_kernel<<<grid, kSelThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
