@@ -124,24 +124,25 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         const int u = step * kStep + slot;
         return (step < n_steps && u < cnt) ? __ldg(lst + u) : -1;
     };
-    auto resolve = [&](int cell) -> int {      // physical page, -1 = masked (absent, bad or not resident)
+    // physical page (< 0 = masked: absent, bad or not resident); the entry is
+    // checked against the pool when it is used, a step after its load
+    auto resolve = [&](int cell) -> int {
         if (cell < 0) return -1;
         if ((cell >> 6) >= a.n_lpages) {
             report(a.dev_status, QSA_DEV_BAD_CELL);
             return -1;
         }
-        const int pp = __ldg(ptab + (cell >> 6));
-        if (pp >= a.n_ppages) {
-            report(a.dev_status, QSA_DEV_BAD_PAGE);
-            return -1;
-        }
-        return pp;
+        return __ldg(ptab + (cell >> 6));
     };
     // Row copies of a step into stage st, and the load of the lane's scale (its
     // FP16 bits, 0 for a masked cell), which put_scale stores one step later, so
     // the load's latency is not waited for in the step that issues it.
     auto issue = [&](int cell, int page, int st) -> uint16_t {
         uint16_t sb = 0;
+        if (page >= a.n_ppages) {
+            report(a.dev_status, QSA_DEV_BAD_PAGE);
+            page = -1;
+        }
         const bool ok = page >= 0;
         if (ok) {
             const size_t row = ((size_t)page * a.n_kv + h) * kPage + (cell & (kPage - 1));
