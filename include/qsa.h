@@ -170,8 +170,11 @@ int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool
  * default, each position gathering its own ~2,051 cells; section Extra Notes
  * times it against the union kernel).  It is the baseline the union path
  * replaces, built on the warp-level tensor path (mma.sync, BF16 in, FP32 sums)
- * with the same K/V handling as qsa_union_attn: exact BF16 K and V, K scale on
- * the score column in FP32, V scale in P.  Arguments and layouts are those of
+ * with the union kernels' K/V handling in BF16: exact BF16 K and V, K scale on
+ * the score column in FP32, V scale in P.  Each (query, KV head) list is split
+ * over four warps whose partial softmax states are merged at the end, so the
+ * summation order differs from a single walk of the list (results agree within
+ * BF16 rounding of the weights).  Arguments and layouts are those of
  * qsa_prompt_attn (sel: [n_q][sel_stride] cells, sel_count: [n_q]); no workspace.
  * The lists need not be sorted.  Device checks as in qsa_union_attn
  * (QSA_DEV_BAD_SEL_COUNT, QSA_DEV_BAD_CELL, QSA_DEV_BAD_PAGE into *dev_status).
