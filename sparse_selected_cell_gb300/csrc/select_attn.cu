@@ -31,8 +31,10 @@
 //     (|int8| <= 127 fits BF16); the K scale (times sm_scale and log2 e)
 //     multiplies each score column in FP32, unselected / masked cells are -inf,
 //     the online softmax runs in the exp2 domain with the same lazy rescale as
-//     the union kernel, and P = p * (V scale) enters O += P V as BF16, with V
-//     converted exactly to a BF16 tile read by ldmatrix.trans.
+//     the union kernel, and P = p * (V scale) enters O += P V as BF16; V also
+//     goes from the INT8 stage straight into the B fragments (ldmatrix.trans of
+//     byte pairs, the output columns permuted so that a lane's accumulators
+//     cover four consecutive dims), so the kernel writes no operand tile.
 #include "qsa_common.cuh"
 
 namespace qsa {
@@ -53,8 +55,6 @@ struct __align__(16) QTile {
 
 struct __align__(16) WarpSmem {
     int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   12 KB
-    uint16_t kb[kStep][kHeadDim];           // BF16 K, then V of the same step: 256-byte rows,      4 KB
-                                            // 16-byte chunks swizzled (swz)
     float ks[kStages][kStep];               // K scale * sm_scale * log2(e); 0 for a masked cell
     float vs[kStages][kStep];               // V scale; 0 for a masked cell
     uint32_t valid[kStages];                // bit c: cell c of the step is selected and resident
@@ -71,6 +71,14 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
+// Four INT8 values in a word -> BF16 pairs (bytes 0, 2) and (bytes 1, 3),
+// exactly, in the way of int8x4_to_bf16.
+__device__ __forceinline__ void int8x4_to_bf16_even_odd(uint32_t w, uint32_t& out02, uint32_t& out13) {
+    const uint32_t l02 = __byte_perm(w, 0x4343u, 0x5240);   // [b0, 0x43, b2, 0x43]
+    const uint32_t l13 = __byte_perm(w, 0x4343u, 0x5341);   // [b1, 0x43, b3, 0x43]
+    out02 = bf16x2_sub(l02 & 0xFF7FFF7Fu, l02 & 0xFF80FF80u);
+    out13 = bf16x2_sub(l13 & 0xFF7FFF7Fu, l13 & 0xFF80FF80u);
+}
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
@@ -83,16 +91,7 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// byte offset of 16-byte chunk `chunk` (0-15) of the 256-byte BF16 row of `cell`.
-// The low three chunk bits are XORed with (cell & 7), so the 8 cells an ldmatrix
-// reads at one chunk hit 8 different bank groups; bit 3 of the chunk (which
-// 128-byte half) also flips bit 2, so the two lanes that store the two halves of
-// one cell's row in the same 8-lane phase hit different bank groups too.
-__device__ __forceinline__ uint32_t swz(int cell, int chunk, int row_bytes) {
-    return (uint32_t)(cell * row_bytes + ((chunk ^ (cell & 7) ^ (((chunk >> 3) & 1) << 2)) << 4));
-}
-
-__global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelArgs a) {
+__global__ void __launch_bounds__(kSelThreads, 4) select_attn_kernel(const SelArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     WarpSmem& s = reinterpret_cast<WarpSmem*>(smem_raw)[warp];
@@ -213,7 +212,8 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
 #pragma unroll
     for (int dt = 0; dt < 16; ++dt) o[dt][0] = o[dt][1] = o[dt][2] = o[dt][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const uint32_t kb_base = smem_u32(&s.kb[0][0]), vb_base = kb_base;   // one tile: K, then V
+    // ldmatrix row of lane l in the V stage: cell (l & 7) + 8 ((l >> 3) & 1), 16-byte chunk 2q + (l >> 4)
+    const int vcell = (lane & 7) + 8 * ((lane >> 3) & 1);
 
 #pragma unroll 1
     for (int step = 0; step < n_steps; ++step) {
@@ -229,22 +229,6 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         cp_async_commit();
         cp_async_wait<kStages - 1>();
         __syncwarp();
-
-        // exact BF16 V tile: lane l converts 64 bytes (half l & 1) of cell (l >> 1)
-        {
-            const int cell = lane >> 1, hh = lane & 1;
-            uint8_t* dst = reinterpret_cast<uint8_t*>(&s.kb[0][0]);
-            const uint8_t* src = reinterpret_cast<const uint8_t*>(&s.raw[st][1][cell][0]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int seg = 4 * hh + k;
-                const uint4 x = *reinterpret_cast<const uint4*>(src + ((seg ^ (cell & 7)) << 4));
-                uint4 lo, hi;
-                int8x16_to_bf16(x, lo, hi);
-                *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg, 256)) = lo;
-                *reinterpret_cast<uint4*>(dst + swz(cell, 2 * seg + 1, 256)) = hi;
-            }
-        }
 
         // S = Q K^T: 16 rows x 16 cells, K straight from the INT8 stage: lane (g, t)
         // of n tile nt reads dims 16kk + 4t .. +3 of cell 8nt + g (one 32-bit word;
@@ -320,19 +304,32 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         }
         l0 = l0 * al0 + ps0;
         l1 = l1 * al1 + ps1;
-        // O += P V: the 16 cells are one k16 step
-        __syncwarp();   // V is in the tile
+        // O += P V: the 16 cells are one k16 step, V straight from the INT8 stage.
+        // ldmatrix.trans on byte pairs: for the 32 dims 32q .. 32q+31, lane (g, t)
+        // gets, of cells 2t, 2t+1 (and 2t+8, 2t+9), the pairs of dims 32q + 2g, +1
+        // and 32q + 16 + 2g, +1.  Bytes 0 and 2 of a word are the two cells' values
+        // of the even dim, bytes 1 and 3 of the odd one: the B operands of two n
+        // tiles whose column g is dim 32q + 2g (tile "even") and 32q + 2g + 1
+        // ("odd").  So O tile 4q + 2h + e holds dims 32q + 16h + 2n + e at column n,
+        // and a lane's accumulators of rows g and g + 8 cover dims 32q + 16h + 4t
+        // .. +3.
         {
-            const int cell = ((lane >> 3) & 1) * 8 + (lane & 7);
+            const uint32_t vrow = smem_u32(&s.raw[st][1][vcell][0]);
 #pragma unroll
-            for (int dn = 0; dn < 16; dn += 2) {
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb_base + swz(cell, dn + (lane >> 4), 256), b0, b1, b2, b3);
-                mma_bf16(o[dn], af, b0, b1);
-                mma_bf16(o[dn + 1], af, b2, b3);
+            for (int q = 0; q < 4; ++q) {
+                uint32_t r[4];
+                ldsm_x4_t(vrow + ((((2 * q + (lane >> 4)) ^ (vcell & 7))) << 4), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    uint32_t e0, d0, e1, d1;
+                    int8x4_to_bf16_even_odd(r[2 * hh], e0, d0);       // cells 2t, 2t+1
+                    int8x4_to_bf16_even_odd(r[2 * hh + 1], e1, d1);   // cells 2t+8, 2t+9
+                    mma_bf16(o[4 * q + 2 * hh], af, e0, e1);
+                    mma_bf16(o[4 * q + 2 * hh + 1], af, d0, d1);
+                }
             }
         }
-        __syncwarp();   // the BF16 tiles are rewritten next step
+        __syncwarp();   // the stage is refilled next step
         c1 = c2;
         c2 = c3;
         p1 = p2;
@@ -354,11 +351,15 @@ __global__ void __launch_bounds__(kSelThreads, 3) select_attn_kernel(const SelAr
         float* pm = po + kSelWarps * 16 * kHeadDim;                      // [warp][16 rows]
         float* pl = pm + kSelWarps * 16;                                 // [warp][16 rows]
 #pragma unroll
-        for (int dt = 0; dt < 16; ++dt) {
-            const int d = dt * 8 + 2 * t4;
-            *reinterpret_cast<float2*>(po + (warp * 16 + r0) * kHeadDim + d) = make_float2(o[dt][0], o[dt][1]);
-            *reinterpret_cast<float2*>(po + (warp * 16 + r1) * kHeadDim + d) = make_float2(o[dt][2], o[dt][3]);
-        }
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int d = 32 * q + 16 * hh + 4 * t4, e = 4 * q + 2 * hh;
+                *reinterpret_cast<float4*>(po + (warp * 16 + r0) * kHeadDim + d) =
+                    make_float4(o[e][0], o[e + 1][0], o[e][1], o[e + 1][1]);
+                *reinterpret_cast<float4*>(po + (warp * 16 + r1) * kHeadDim + d) =
+                    make_float4(o[e][2], o[e + 1][2], o[e][3], o[e + 1][3]);
+            }
         if (t4 == 0) {
             pm[warp * 16 + r0] = m0;
             pm[warp * 16 + r1] = m1;
