@@ -71,6 +71,15 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
+// Position of 16-byte chunk c of a cell's 128-byte row in the INT8 stage: c XOR
+// f(cell), f(cell) = 4 (cell & 1) + ((cell >> 1) & 3).  f takes 8 different
+// values over 8 consecutive cells, so an ldmatrix over 8 cells at one chunk hits
+// 8 bank groups; and two neighbouring cells differ in bit 2 of f, so the 16-byte
+// K reads of two cells (chunks 0-3 or 4-7 of each) fill all 8 bank groups.
+__device__ __forceinline__ uint32_t stage_chunk(int c, int cell) {
+    return (uint32_t)(c ^ (((cell & 1) << 2) | ((cell >> 1) & 3)));
+}
+
 // Four INT8 values in a word -> BF16 pairs (bytes 0, 2) and (bytes 1, 3),
 // exactly, in the way of int8x4_to_bf16.
 __device__ __forceinline__ void int8x4_to_bf16_even_odd(uint32_t w, uint32_t& out02, uint32_t& out13) {
@@ -148,7 +157,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_attn_kernel(const SelAr
             const int8_t* src = (kv ? a.v_pool : a.k_pool) + row * kHeadDim;
             const uint32_t dst = smem_u32(&s.raw[st][kv][slot][0]);
 #pragma unroll
-            for (int seg = 0; seg < 8; ++seg) cp_async16(dst + ((seg ^ (slot & 7)) << 4), src + seg * 16);
+            for (int seg = 0; seg < 8; ++seg) cp_async16(dst + (stage_chunk(seg, slot) << 4), src + seg * 16);
             sb = __ldg((kv ? a.v_scale : a.k_scale) + row);
         }
         const uint32_t vm = __ballot_sync(0xffffffffu, ok) & 0xFFFFu;
@@ -176,25 +185,24 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_attn_kernel(const SelAr
     uint16_t sb_next = 0;   // scale of step + kStages - 2 (loaded one step ago), stored at the next step's top
 
     // ---- Q (A operand of S, BF16), rows 0-11: the KV head's 12 query heads.  The
-    // head dimension is permuted inside each 16-wide k step, for Q and K alike (a
-    // dot product does not depend on the order of its terms): logical entries
-    // 2t, 2t+1, 2t+8, 2t+9 of a k step -- what lane (g, t) holds of an m16n8k16
-    // fragment -- are dims 16kk + 4t .. 16kk + 4t + 3, so a lane's K operand is
-    // one 32-bit word of the INT8 row.  Thread t of the CTA stores row t >> 3,
-    // k step t & 7 (16 dims).
+    // head dimension is permuted, for Q and K alike (a dot product does not
+    // depend on the order of its terms): in k step kk = 4hk + k' (hk, k' < 4 ...),
+    // the logical entries 2t, 2t+1, 2t+8, 2t+9 -- what lane (g, t) holds of an
+    // m16n8k16 fragment -- are dims 64hk + 16t + 4k' .. +3.  So a lane's K operands
+    // of four k steps are one 16-byte piece of the INT8 row (bytes 64hk + 16t ..
+    // +15).  Thread t of the CTA stores row t >> 3, k step t & 7.
     {
         const int row = threadIdx.x >> 3, kk = threadIdx.x & 7;
         const bool live = row < kHeadsPerKv;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((size_t)i * n_heads + h * kHeadsPerKv + (live ? row : 0)) * kHeadDim + 16 * kk);
-        uint4 x[2] = {live ? __ldg(src) : make_uint4(0u, 0u, 0u, 0u), live ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u)};
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(x);
-        // logical position j of physical dim p = 4t + 2hi + b (b, hi in {0, 1}): j = 2t + b + 8hi
+        const uint16_t* qsrc = a.q + ((size_t)i * n_heads + h * kHeadsPerKv + (live ? row : 0)) * kHeadDim +
+                             64 * (kk >> 2) + 4 * (kk & 3);
+        // logical pair (2t, 2t+1) is dims +16t, +16t+1; pair (2t+8, 2t+9) dims +16t+2, +16t+3
         uint32_t lg[8];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-            lg[t] = w[2 * t];            // dims 4t, 4t+1
-            lg[4 + t] = w[2 * t + 1];    // dims 4t+2, 4t+3
+            const uint2 x = live ? __ldg(reinterpret_cast<const uint2*>(qsrc + 16 * t)) : make_uint2(0u, 0u);
+            lg[t] = x.x;
+            lg[4 + t] = x.y;
         }
         uint8_t* qrow = reinterpret_cast<uint8_t*>(&qt.q[row][0]);
         *reinterpret_cast<uint4*>(qrow + (((2 * kk) ^ (row & 7)) << 4)) = make_uint4(lg[0], lg[1], lg[2], lg[3]);
@@ -236,22 +244,34 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_attn_kernel(const SelAr
         // 32 different banks) and converts them exactly to two FP16 pairs.  Even and
         // odd k steps accumulate separately (two shorter dependency chains).
         float sc[2][4];
+        {
+            // lane (g, t): the 16-byte pieces t and 4 + t of cells g and 8 + g (k steps 0-3, 4-7)
+            uint4 kw[2][2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            const int cell = nt * 8 + g4;
-            const uint8_t* krow = reinterpret_cast<const uint8_t*>(&s.raw[st][0][cell][0]) + 4 * t4;
+            for (int nt = 0; nt < 2; ++nt) {
+                const int cell = nt * 8 + g4;
+                const uint8_t* krow = reinterpret_cast<const uint8_t*>(&s.raw[st][0][cell][0]);
+                kw[nt][0] = *reinterpret_cast<const uint4*>(krow + (stage_chunk(t4, cell) << 4));
+                kw[nt][1] = *reinterpret_cast<const uint4*>(krow + (stage_chunk(4 + t4, cell) << 4));
+            }
+            float acc[2][2][4] = {};   // [n tile][k step parity]: two shorter dependency chains each
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint32_t qa[4];
                 ldsm_x4(q_base + (((2 * kk + (lane >> 4)) ^ (qr & 7)) << 4), qa[0], qa[1], qa[2], qa[3]);
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(krow + ((kk ^ (cell & 7)) << 4));
-                uint32_t b0, b1;
-                int8x4_to_bf16(w, b0, b1);
-                mma_bf16(acc[kk & 1], qa, b0, b1);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint4 v4 = kw[nt][kk >> 2];
+                    const uint32_t w = (kk & 3) == 0 ? v4.x : (kk & 3) == 1 ? v4.y : (kk & 3) == 2 ? v4.z : v4.w;
+                    uint32_t b0, b1;
+                    int8x4_to_bf16(w, b0, b1);
+                    mma_bf16(acc[nt][kk & 1], qa, b0, b1);
+                }
             }
 #pragma unroll
-            for (int v = 0; v < 4; ++v) sc[nt][v] = acc[0][v] + acc[1][v];
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) sc[nt][v] = acc[nt][0][v] + acc[nt][1][v];
         }
         // column scale (log2 domain), masked cells -inf
         const uint32_t vm = s.valid[st];
@@ -318,7 +338,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_attn_kernel(const SelAr
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t r[4];
-                ldsm_x4_t(vrow + ((((2 * q + (lane >> 4)) ^ (vcell & 7))) << 4), r[0], r[1], r[2], r[3]);
+                ldsm_x4_t(vrow + (stage_chunk(2 * q + (lane >> 4), vcell) << 4), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     uint32_t e0, d0, e1, d1;
