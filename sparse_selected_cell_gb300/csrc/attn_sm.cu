@@ -233,9 +233,25 @@ __device__ __forceinline__ void leave_all(int set, int quad) {
 // column of the masks, and the warp appends them in cell order (a prefix count
 // over the OR).  Lists must be strictly increasing, as the launch pair's
 // contract states; each list is read once.
+// The next entries of one list, read by the whole warp: e1 = entry cursor + lane,
+// e2 = entry cursor + 32 + lane, e3 = entry cursor + 64 (the same for every lane);
+// INT32_MAX past the list's end.  A page holds at most 64 of a list's cells, so
+// one such read decides a page for the list and finds the list's next cell.
+struct ListBatch {
+    int32_t e1, e2, e3;
+};
+__device__ __forceinline__ ListBatch read_list(const int32_t* list, int cur, int cnt, int lane) {
+    ListBatch b;
+    b.e1 = cur + lane < cnt ? __ldg(list + cur + lane) : INT32_MAX;
+    b.e2 = cur + 32 + lane < cnt ? __ldg(list + cur + 32 + lane) : INT32_MAX;
+    b.e3 = cur + 64 < cnt ? __ldg(list + cur + 64) : INT32_MAX;
+    return b;
+}
+
 __device__ void union_role(const Ctx& c, int lane) {
     const AttnArgs& a = *c.a;
     UnionRing* R = c.ring;
+    // lane j < nj: list j's count, cursor and next cell (INT32_MAX at its end)
     int cnt = 0, cursor = 0, head = INT32_MAX;
     const int32_t* list = a.sel;
     if (lane < c.nj) {
@@ -248,35 +264,78 @@ __device__ void union_role(const Ctx& c, int lane) {
         list = a.sel + (size_t)q * a.sel_stride;
         head = cnt > 0 ? __ldg(list) : INT32_MAX;
     }
+    // entries cursor + 63, + 64, + 127 and + 128 of the lane's list, read as soon
+    // as the cursor moves, so that the next two whole-page checks find theirs loaded
+    int32_t e63 = INT32_MAX, e64 = INT32_MAX, e127 = INT32_MAX, e128 = INT32_MAX;
+    auto entry = [&](int u) { return u < cnt ? __ldg(list + u) : INT32_MAX; };
+    auto look_ahead = [&]() {
+        e63 = entry(cursor + 63);
+        e64 = entry(cursor + 64);
+        e127 = entry(cursor + 127);
+        e128 = entry(cursor + 128);
+    };
+    if (lane < c.nj) look_ahead();
+    const int32_t* lists = a.sel + (size_t)c.q_begin * a.sel_stride;
     int produced = 0;
     for (;;) {
         const int pl = head == INT32_MAX ? INT32_MAX : (head >> 6);   // page of the list's next cell
         const int p = __reduce_min_sync(0xffffffffu, pl);
         if (p == INT32_MAX) break;
-        uint32_t wlo = 0, whi = 0;
-        if (pl == p) {
-            const int base = head - (head & 63);
-            const bool whole = head == base && cursor + 63 < cnt && __ldg(list + cursor + 63) == base + 63;
-            if (whole) {
-                wlo = whi = 0xffffffffu;
-                cursor += 64;
-                head = cursor < cnt ? __ldg(list + cursor) : INT32_MAX;
-            } else {
-                while (head != INT32_MAX && (head >> 6) == p) {
-                    const int b = head & 63;
-                    if (b < 32) wlo |= 1u << b;
-                    else whi |= 1u << (b - 32);
-                    ++cursor;
-                    head = cursor < cnt ? __ldg(list + cursor) : INT32_MAX;
-                }
-            }
+        // Whole pages, all lists at once: a list holds all of page p when its next
+        // cell is the page's first and the entry 63 places on is the page's last.
+        const bool mine = pl == p;
+        const int base = p << 6;
+        const bool whole = mine && head == base && e63 == base + 63;
+        if (whole) {
+            cursor += 64;
+            head = e64;
+            e63 = e127;
+            e64 = e128;
+            e127 = entry(cursor + 127);
+            e128 = entry(cursor + 128);
         }
-        const uint32_t olo = __reduce_or_sync(0xffffffffu, wlo), ohi = __reduce_or_sync(0xffffffffu, whi);
-        uint32_t m0 = 0, m1 = 0;   // masks of cells 64p + lane and 64p + 32 + lane
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j) {
-            m0 |= ((__shfl_sync(0xffffffffu, wlo, j) >> lane) & 1u) << j;
-            m1 |= ((__shfl_sync(0xffffffffu, whi, j) >> lane) & 1u) << j;
+        const uint32_t wholes = __ballot_sync(0xffffffffu, whole);   // bit j: list j holds all of page p
+        uint32_t olo = wholes ? 0xffffffffu : 0u, ohi = olo;        // union cells of the page (lo: 64p + b)
+        uint32_t m0 = wholes, m1 = wholes;                           // masks of cells 64p + lane, 64p + 32 + lane
+        // Lists that hold part of page p, one after another, each read by the whole
+        // warp (64 entries and the one after them in one round trip); the next
+        // list's read is issued before the current one is taken apart.
+        uint32_t part = __ballot_sync(0xffffffffu, mine && !whole);
+        if (part) {
+            int j = __ffs(part) - 1;
+            ListBatch cur = read_list(lists + (size_t)j * a.sel_stride, __shfl_sync(0xffffffffu, cursor, j),
+                                      __shfl_sync(0xffffffffu, cnt, j), lane);
+            for (;;) {
+                part &= part - 1;
+                const int jn = part ? __ffs(part) - 1 : -1;
+                ListBatch nxt = cur;
+                if (jn >= 0)
+                    nxt = read_list(lists + (size_t)jn * a.sel_stride, __shfl_sync(0xffffffffu, cursor, jn),
+                                    __shfl_sync(0xffffffffu, cnt, jn), lane);
+                // list j's cells in page p are a prefix of its remaining entries
+                const bool in1 = cur.e1 != INT32_MAX && (cur.e1 >> 6) == p;
+                const bool in2 = cur.e2 != INT32_MAX && (cur.e2 >> 6) == p;
+                const int k = __popc(__ballot_sync(0xffffffffu, in1)) + __popc(__ballot_sync(0xffffffffu, in2));
+                const uint32_t b1 = in1 ? 1u << (cur.e1 & 31) : 0u, b2 = in2 ? 1u << (cur.e2 & 31) : 0u;
+                const uint32_t wlo =
+                    __reduce_or_sync(0xffffffffu, ((cur.e1 & 32) ? 0u : b1) | ((cur.e2 & 32) ? 0u : b2));
+                const uint32_t whi =
+                    __reduce_or_sync(0xffffffffu, ((cur.e1 & 32) ? b1 : 0u) | ((cur.e2 & 32) ? b2 : 0u));
+                const int32_t nc = k < 32 ? __shfl_sync(0xffffffffu, cur.e1, k & 31)
+                                          : (k < 64 ? __shfl_sync(0xffffffffu, cur.e2, k & 31) : cur.e3);
+                if (lane == j) {
+                    cursor += k;
+                    head = nc;
+                    look_ahead();
+                }
+                olo |= wlo;
+                ohi |= whi;
+                m0 |= ((wlo >> lane) & 1u) << j;
+                m1 |= ((whi >> lane) & 1u) << j;
+                if (jn < 0) break;
+                cur = nxt;
+                j = jn;
+            }
         }
         const int n_lo = __popc(olo), n_new = n_lo + __popc(ohi);
         // room in the ring: no producer may still need the slots about to be reused
