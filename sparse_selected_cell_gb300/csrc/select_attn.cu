@@ -46,7 +46,7 @@ constexpr int kStep = 16;                  // cells per step
 constexpr int kStages = 2;                 // INT8 stage ring: copies run kStages - 1 steps ahead
 constexpr float kSelRescaleLog2 = 32.f;    // lazy rescale threshold (exp2 domain), as in attn_tc.cu
 
-// The (query, KV head)'s 12 query-head rows as FP16 (rows 12-15 zero), shared by
+// The (query, KV head)'s 12 query-head rows as BF16 (rows 12-15 zero), shared by
 // the CTA's four warps: 256-byte rows, 16-byte chunks XOR-swizzled by (row & 7),
 // each 16-wide k step in the permuted order the S fragments use (see below).
 struct __align__(16) QTile {
@@ -54,7 +54,7 @@ struct __align__(16) QTile {
 };
 
 struct __align__(16) WarpSmem {
-    int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunks XOR (cell & 7)   12 KB
+    int8_t raw[kStages][2][kStep][kHeadDim];   // [stage][K|V][cell][d], 16-byte chunk c at stage_chunk(c, cell); 8 KB
     float ks[kStages][kStep];               // K scale * sm_scale * log2(e); 0 for a masked cell
     float vs[kStages][kStep];               // V scale; 0 for a masked cell
     uint32_t valid[kStages];                // bit c: cell c of the step is selected and resident
@@ -239,10 +239,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_attn_kernel(const SelAr
         __syncwarp();
 
         // S = Q K^T: 16 rows x 16 cells, K straight from the INT8 stage: lane (g, t)
-        // of n tile nt reads dims 16kk + 4t .. +3 of cell 8nt + g (one 32-bit word;
-        // the stage's 16-byte chunks are XOR-swizzled by cell, so the 32 lanes hit
-        // 32 different banks) and converts them exactly to two FP16 pairs.  Even and
-        // odd k steps accumulate separately (two shorter dependency chains).
+        // of n tile nt reads, for k steps 4hk .. 4hk + 3, bytes 64hk + 16t .. +15 of
+        // cell 8nt + g (one 16-byte load; one 32-bit word per k step) and converts
+        // each word exactly to two BF16 pairs.  Even and odd k steps accumulate
+        // separately (two shorter dependency chains).
         float sc[2][4];
         {
             // lane (g, t): the 16-byte pieces t and 4 + t of cells g and 8 + g (k steps 0-3, 4-7)
