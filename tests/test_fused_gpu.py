@@ -136,3 +136,37 @@ def test_fused_bad_counts_are_clamped_and_reported(qsa):
     assert st_f & 1                      # QSA_DEV_BAD_SEL_COUNT
     assert np.isfinite(fused).all()
     assert (fused[3] == 0).all()         # clamped to an empty list
+
+
+def test_fused_mixed_whole_and_partial_pages(qsa):
+    """Lists that mix whole pages with pages they hold only in part, at every
+    density, several lists sharing a page while holding different parts of it, up
+    to the 2,051-cell cap: the union builder's whole-page checks (all lists at
+    once) and its batched reads of partly held pages, against the launch pair bit
+    for bit and against the oracle."""
+    w = gen.make(2, n_q=64)          # 4,096-cell context: pages 0-63
+    rng = np.random.default_rng(23)
+    shared = sorted(rng.choice(64, size=20, replace=False).tolist())   # pages several lists touch
+
+    def one_list(i):
+        cells = []
+        for p in range(64):
+            if p in shared and rng.random() < 0.7:
+                mode = rng.integers(0, 3)
+            elif rng.random() < 0.25:
+                mode = rng.integers(0, 3)
+            else:
+                continue
+            if mode == 0:                                  # the whole page
+                cells += range(64 * p, 64 * p + 64)
+            else:                                          # part of it, sparse or dense
+                k = int(rng.integers(1, 12)) if mode == 1 else int(rng.integers(40, 64))
+                cells += sorted((64 * p + rng.choice(64, size=k, replace=False)).tolist())
+        return cells[:2051]
+
+    sel, cnt = _lists(w, [one_list(i) for i in range(w.n_q)])
+    fused, pair, st_f, st_p = run_both(qsa, w, sel=sel, sel_count=cnt)
+    assert st_f == 0 and st_p == 0
+    assert np.array_equal(fused, pair)
+    ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, sel, cnt, w.n_kv, w.sm_scale)
+    check_close(fused, ref, "mixed pages")
