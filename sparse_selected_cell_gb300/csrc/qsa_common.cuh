@@ -22,11 +22,8 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
     if (status) atomicOr(status, bits);
 }
 
-// ---------------------------------------------------------------- int8 -> bf16
-// Four signed bytes are widened to exact floats with the 2^23 trick: the byte
-// biased by 128 becomes the low mantissa bits of 2^23, and subtracting
-// 2^23 + 128 leaves the integer.  Scaling happens in FP32 and each pair is then
-// rounded to bf16x2 once (round to nearest even).
+// ---------------------------------------------------------------- conversions
+// FP32 pairs rounded (to nearest even) into packed 16-bit pairs, low half first.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -39,21 +36,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-__device__ __forceinline__ void dequant4(uint32_t w, float scale, uint32_t& out01, uint32_t& out23) {
-    const uint32_t u = w ^ 0x80808080u;
-    const float bias = 8388736.0f;   // 2^23 + 128
-    float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7540)),
-                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7541)));
-    float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7542)),
-                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7543)));
-    const float2 nb = make_float2(-bias, -bias);
-    const float2 s2 = make_float2(scale, scale);
-    a = __fmul2_rn(__fadd2_rn(a, nb), s2);
-    b = __fmul2_rn(__fadd2_rn(b, nb), s2);
-    out01 = pack_bf16x2(a.x, a.y);
-    out23 = pack_bf16x2(b.x, b.y);
-}
 
 // Exact int8 -> bf16 (|x| <= 128 fits bf16's 8-bit significand).  Each byte b
 // sits in the low byte of a 16-bit lane whose high byte is 0x43: keeping b's low
@@ -86,37 +68,6 @@ __device__ __forceinline__ void int8x4_to_f16(uint32_t w, uint32_t& out01, uint3
     const uint32_t u = w ^ 0x80808080u;
     out01 = f16x2_sub(__byte_perm(u, 0x6464u, 0x5140), 0x64806480u);   // [u0, 0x64, u1, 0x64]
     out23 = f16x2_sub(__byte_perm(u, 0x6464u, 0x5342), 0x64806480u);   // [u2, 0x64, u3, 0x64]
-}
-
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// Dequantisation of four INT8 values to FP16 with one FP16 scale s (held in both
-// halves of s2): the exact integers above times s, each product rounded to FP16
-// once (round to nearest even).
-__device__ __forceinline__ void int8x4_to_f16_scaled(uint32_t w, uint32_t s2, uint32_t& out01, uint32_t& out23) {
-    uint32_t a, b;
-    int8x4_to_f16(w, a, b);
-    out01 = f16x2_mul(a, s2);
-    out23 = f16x2_mul(b, s2);
-}
-
-__device__ __forceinline__ void int8x16_to_bf16(uint4 raw, uint4& lo, uint4& hi) {
-    int8x4_to_bf16(raw.x, lo.x, lo.y);
-    int8x4_to_bf16(raw.y, lo.z, lo.w);
-    int8x4_to_bf16(raw.z, hi.x, hi.y);
-    int8x4_to_bf16(raw.w, hi.z, hi.w);
-}
-
-// 16 int8 values -> 16 bf16 values (two 16-byte words), times `scale`.
-__device__ __forceinline__ void dequant16(uint4 raw, float scale, uint4& lo, uint4& hi) {
-    dequant4(raw.x, scale, lo.x, lo.y);
-    dequant4(raw.y, scale, lo.z, lo.w);
-    dequant4(raw.z, scale, hi.x, hi.y);
-    dequant4(raw.w, scale, hi.z, hi.w);
 }
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
