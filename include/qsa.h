@@ -149,13 +149,17 @@ int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
  * positions' sorted selections; section What changed: there the union and the
  * attention run as a launch pair).  No union arrays reach global memory and no
  * workspace is needed.  The result is that of qsa_prompt_attn with
- * variant = QSA_ATTN_TCGEN05_SM, bit for bit: a union-builder warp merges the
- * group's 8 lists page by page into a shared-memory ring, and the attention
- * pipeline takes its chunks from there in the same placement.
+ * variant = QSA_ATTN_TCGEN05_SM, bit for bit: each CTA first builds its group's
+ * union in shared memory with the union kernel's own algorithm, then runs that
+ * variant's attention pipeline on it.
  *   - Arguments and layouts are those of qsa_prompt_attn without the workspace,
  *     union stride and variant.  Lists must be strictly increasing (the union
  *     build's precondition); counts outside [0, sel_stride] are clamped and
  *     reported as QSA_DEV_BAD_SEL_COUNT.  Device checks as in qsa_union_attn.
+ *   - The union of 8 lists (up to 8 x sel_stride entries, 5 bytes each) must fit
+ *     the CTA's shared memory next to the pipeline's: sel_stride up to about
+ *     2,700 on GB300 (2,056 holds the method's 2,051-cell cap); QSA_ERR_UNSUPPORTED
+ *     above that.
  *   - n_q == 0 returns QSA_OK with no launch. */
 int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
                    const uint16_t* k_scale, const uint16_t* v_scale,

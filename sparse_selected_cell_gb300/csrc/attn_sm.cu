@@ -46,10 +46,13 @@
 //              row and thread of the chunk's INT8 rows, issued two chunks ahead
 //              into registers, converted exactly to FP16 straight into operand
 //              tiles in the 128-byte swizzled layouts the tensor core reads.
-//   warp 24    (fused path only) union builder: merges the 8 sorted lists page
-//              by page into a shared-memory ring of (cell, 8-bit mask) entries
-//              in increasing cell order, which the producers read in place of the
-//              union arrays.
+// Fused path: before the pipeline starts, the whole CTA builds the group's
+//              union into shared memory with the union kernel's own build
+//              (union_core.cuh: a byte map per window of cells, marking, a page
+//              scan and an ordered compaction), the byte map in the K/V tile
+//              area and its small arrays in the table ring, not yet in use; the
+//              producers then read the union from there in place of the union
+//              arrays.
 // The chunk placement, the tables and every product are the same in both
 // paths, so the fused path's output equals the launch pair's bit for bit.
 // Precision.  K and V enter the products exactly; the K scale multiplies the
@@ -64,20 +67,19 @@
 // the MMAs they started, and the CTA frees its Tensor Memory and exits.
 #include "qsa_common.cuh"
 #include "tc_ptx.cuh"
+#include "union_core.cuh"
 
 namespace qsa {
 namespace {
 
 constexpr int kWarpProducer0 = 3, kWarpProducer1 = 22;   // even / odd chunks
 constexpr int kWarpMmaS = 7, kWarpMmaPV = 23;             // S issuer, P V issuer
-constexpr int kWarpUnion = 24;                            // fused path only
 constexpr int kLoadThreads = 128;            // per loader group (K or V)
 constexpr int kSetWarps = 6;                 // softmax warps per set
 constexpr int kNS = 16;                      // per-chunk table ring
 constexpr int kNSb = 4;                      // S/P buffers in TMEM
 constexpr int kNK = 3;                       // K tiles
 constexpr int kNV = 3;                       // V tiles
-constexpr int kRing = 1024;                  // union entries kept by the fused path's builder
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColQ = 0, kColO = 64, kColS = 192;   // S buffer b at kColS + 64 b
 // Lazy rescale threshold (exp2 domain): the running max only moves, and O is
@@ -87,8 +89,7 @@ constexpr uint32_t kColQ = 0, kColO = 64, kColS = 192;   // S buffer b at kColS 
 constexpr float kRescaleLog2 = 12.f;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
-template <bool kFused>
-constexpr int num_warps() { return kFused ? 25 : 24; }
+constexpr int kWarps = 24;
 
 __device__ __forceinline__ int k_loader_index(int warp) { return warp - 16; }   // warps 16-19
 __device__ __forceinline__ int v_loader_index(int warp) {                      // warps 20, 21, 11, 15
@@ -106,21 +107,6 @@ struct RawTab {
     int32_t pad;
 };
 
-// The fused path's union ring: entry u (in increasing cell order) at slot
-// u % kRing, and the first 64 entries also in `first` (the chunk placement reads
-// them again at the end).  `produced` entries are written; `done` is set, with
-// `total` the union size, when the lists are exhausted; cons[p] is the first
-// entry producer p may still read.
-struct UnionRing {
-    int32_t cell[kRing];
-    uint8_t mask[kRing];
-    int32_t first_cell[kChunk];
-    uint8_t first_mask[kChunk];
-    int32_t produced, done, total, pad0;
-    int32_t cons[2];
-    int32_t pad1[2];
-};
-
 constexpr uint32_t kTileBytes = kChunk * kHeadDim * 2;   // 16 KB FP16 K or V tile (two 64-column halves)
 constexpr uint32_t kOffKb = 0;
 constexpr uint32_t kOffVb = kOffKb + kNK * kTileBytes;
@@ -132,8 +118,7 @@ constexpr uint32_t kOffXchg = kOffRawTab + kNS * (uint32_t)sizeof(RawTab);
 constexpr uint32_t kOffMslot = kOffXchg + 8 * kRows * 4;
 constexpr uint32_t kOffLsum = kOffMslot + 2 * kRows * 4;
 constexpr uint32_t kOffRs = kOffLsum + 4 * kRows * 4;
-constexpr uint32_t kOffRing = (kOffRs + kRows * 4 + 15u) & ~15u;
-constexpr uint32_t kOffBars = (kOffRing + (uint32_t)sizeof(UnionRing) + 7u) & ~7u;
+constexpr uint32_t kOffBars = (kOffRs + kRows * 4 + 7u) & ~7u;
 // K_EMPTY[b]: S(t) with t % kNK == b has read K tile b.  S_FULL[b]: S(t), t % 4
 // == b, is in S buffer b.  P_READY[b]: P(t) is in S buffer b (or, at t = the
 // chunk count, the stream has ended).  V_EMPTY[b]: P(t) V with t % kNV == b
@@ -150,7 +135,16 @@ enum { BAR_TAB_FULL = 0, BAR_TAB_EMPTY = kNS, BAR_K_FULL = 2 * kNS, BAR_K_EMPTY 
 constexpr uint32_t kOffMisc = kOffBars + NUM_BARS * 8;      // tmem base, abort flag, chunk count
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;           // + alignment slack
-static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+// The fused path keeps its group's union after that: cells (int32) then masks (uint8).
+constexpr uint32_t kOffUnion = (kSmemUsed + 15u) & ~15u;
+// While the union is built (before any tile or table is used), the byte map of
+// its window sits in the K/V tile area and its small arrays in the table ring.
+static_assert(kNK * kTileBytes + kNV * kTileBytes >= (uint32_t)kUnionWindow, "byte map fits the tile area");
+constexpr uint32_t kUnionSmallBytes = kUnionPages + 2 * kUnionPages + 5 * kGroup * 4 + kWarps * 4;
+static_assert(kNS * sizeof(RawTab) >= kUnionSmallBytes, "union scratch fits the table ring");
+__host__ __device__ constexpr uint32_t fused_union_capacity(int sel_stride) {
+    return ((uint32_t)kGroup * (uint32_t)sel_stride + 15u) & ~15u;
+}
 
 struct Ctx {
     const AttnArgs* a;
@@ -158,11 +152,11 @@ struct Ctx {
     uint32_t base_u;
     uint32_t tmem;
     volatile int* abort_flag;
-    volatile int* n_final;   // the chunk count, once the stream's end is known
-    UnionRing* ring;         // fused path
-    int g, h, nj, q_begin, n_heads, U, n_chunks;   // U, n_chunks: launch-pair path only
+    volatile int* n_final;   // the chunk count
+    const int32_t* ucell;    // the group's union: cells and masks (global memory, or shared on the fused path)
+    const uint8_t* umask;
+    int g, h, nj, q_begin, n_heads, U, n_chunks;
     float kmul;
-    bool fused;
 };
 
 __device__ __forceinline__ uint32_t bar(const Ctx& c, int i) { return c.base_u + kOffBars + 8u * i; }
@@ -175,27 +169,6 @@ __device__ __forceinline__ bool wait_addr(const Ctx& c, uint32_t addr, uint32_t 
     if (tc::mbar_wait(addr, parity, c.abort_flag, kWaitNs)) return true;
     report(c.a->dev_status, QSA_DEV_WAIT_TIMEOUT);
     return false;
-}
-
-// Bounded wait until *flag_a >= need or *flag_b != 0 (shared-memory progress
-// counters of the fused path); false after an abort or when the time limit ran
-// out (then it sets the abort flag and the timeout bit itself).
-__device__ __forceinline__ bool wait_progress(const Ctx& c, const volatile int32_t* flag_a, int need,
-                                              const volatile int32_t* flag_b) {
-    if (*flag_a >= need || *flag_b != 0) return true;
-    const uint64_t t0 = tc::globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        __nanosleep(32);
-        if (*flag_a >= need || *flag_b != 0) return true;
-        if ((it & 15u) == 0) {
-            if (*c.abort_flag) return false;
-            if (tc::globaltimer_ns() - t0 > kWaitNs) {
-                *c.abort_flag = 1;
-                report(c.a->dev_status, QSA_DEV_WAIT_TIMEOUT);
-                return false;
-            }
-        }
-    }
 }
 
 // Named barriers (immediate ids): 1 + 3*set + quad for the two warps of a set
@@ -225,160 +198,6 @@ __device__ __forceinline__ void leave_all(int set, int quad) {
     named_arrive<128>(7 + quad);
 }
 
-// ------------------------------------------------------------------ union builder (fused path)
-// Lane j < 8 walks query j's sorted list.  Each step takes the lowest page p
-// any list still reaches, and each list on p contributes the 64-bit mask of its
-// cells in p (a whole page is recognised from its first and 64th entries).  The
-// union's cells in p are the OR of the masks, each cell's 8-bit mask is the
-// column of the masks, and the warp appends them in cell order (a prefix count
-// over the OR).  Lists must be strictly increasing, as the launch pair's
-// contract states; each list is read once.
-// The next entries of one list, read by the whole warp: e1 = entry cursor + lane,
-// e2 = entry cursor + 32 + lane, e3 = entry cursor + 64 (the same for every lane);
-// INT32_MAX past the list's end.  A page holds at most 64 of a list's cells, so
-// one such read decides a page for the list and finds the list's next cell.
-struct ListBatch {
-    int32_t e1, e2, e3;
-};
-__device__ __forceinline__ ListBatch read_list(const int32_t* list, int cur, int cnt, int lane) {
-    ListBatch b;
-    b.e1 = cur + lane < cnt ? __ldg(list + cur + lane) : INT32_MAX;
-    b.e2 = cur + 32 + lane < cnt ? __ldg(list + cur + 32 + lane) : INT32_MAX;
-    b.e3 = cur + 64 < cnt ? __ldg(list + cur + 64) : INT32_MAX;
-    return b;
-}
-
-__device__ void union_role(const Ctx& c, int lane) {
-    const AttnArgs& a = *c.a;
-    UnionRing* R = c.ring;
-    // lane j < nj: list j's count, cursor and next cell (INT32_MAX at its end)
-    int cnt = 0, cursor = 0, head = INT32_MAX;
-    const int32_t* list = a.sel;
-    if (lane < c.nj) {
-        const int q = c.q_begin + lane;
-        cnt = __ldg(a.sel_count + q);
-        if (cnt < 0 || cnt > a.sel_stride) {
-            report(a.dev_status, QSA_DEV_BAD_SEL_COUNT);
-            cnt = cnt < 0 ? 0 : a.sel_stride;
-        }
-        list = a.sel + (size_t)q * a.sel_stride;
-        head = cnt > 0 ? __ldg(list) : INT32_MAX;
-    }
-    // entries cursor + 63, + 64, + 127 and + 128 of the lane's list, read as soon
-    // as the cursor moves, so that the next two whole-page checks find theirs loaded
-    int32_t e63 = INT32_MAX, e64 = INT32_MAX, e127 = INT32_MAX, e128 = INT32_MAX;
-    auto entry = [&](int u) { return u < cnt ? __ldg(list + u) : INT32_MAX; };
-    auto look_ahead = [&]() {
-        e63 = entry(cursor + 63);
-        e64 = entry(cursor + 64);
-        e127 = entry(cursor + 127);
-        e128 = entry(cursor + 128);
-    };
-    if (lane < c.nj) look_ahead();
-    const int32_t* lists = a.sel + (size_t)c.q_begin * a.sel_stride;
-    int produced = 0;
-    for (;;) {
-        const int pl = head == INT32_MAX ? INT32_MAX : (head >> 6);   // page of the list's next cell
-        const int p = __reduce_min_sync(0xffffffffu, pl);
-        if (p == INT32_MAX) break;
-        // Whole pages, all lists at once: a list holds all of page p when its next
-        // cell is the page's first and the entry 63 places on is the page's last.
-        const bool mine = pl == p;
-        const int base = p << 6;
-        const bool whole = mine && head == base && e63 == base + 63;
-        if (whole) {
-            cursor += 64;
-            head = e64;
-            e63 = e127;
-            e64 = e128;
-            e127 = entry(cursor + 127);
-            e128 = entry(cursor + 128);
-        }
-        const uint32_t wholes = __ballot_sync(0xffffffffu, whole);   // bit j: list j holds all of page p
-        uint32_t olo = wholes ? 0xffffffffu : 0u, ohi = olo;        // union cells of the page (lo: 64p + b)
-        uint32_t m0 = wholes, m1 = wholes;                           // masks of cells 64p + lane, 64p + 32 + lane
-        // Lists that hold part of page p, one after another, each read by the whole
-        // warp (64 entries and the one after them in one round trip); the next
-        // list's read is issued before the current one is taken apart.
-        uint32_t part = __ballot_sync(0xffffffffu, mine && !whole);
-        if (part) {
-            int j = __ffs(part) - 1;
-            ListBatch cur = read_list(lists + (size_t)j * a.sel_stride, __shfl_sync(0xffffffffu, cursor, j),
-                                      __shfl_sync(0xffffffffu, cnt, j), lane);
-            for (;;) {
-                part &= part - 1;
-                const int jn = part ? __ffs(part) - 1 : -1;
-                ListBatch nxt = cur;
-                if (jn >= 0)
-                    nxt = read_list(lists + (size_t)jn * a.sel_stride, __shfl_sync(0xffffffffu, cursor, jn),
-                                    __shfl_sync(0xffffffffu, cnt, jn), lane);
-                // list j's cells in page p are a prefix of its remaining entries
-                const bool in1 = cur.e1 != INT32_MAX && (cur.e1 >> 6) == p;
-                const bool in2 = cur.e2 != INT32_MAX && (cur.e2 >> 6) == p;
-                const int k = __popc(__ballot_sync(0xffffffffu, in1)) + __popc(__ballot_sync(0xffffffffu, in2));
-                const uint32_t b1 = in1 ? 1u << (cur.e1 & 31) : 0u, b2 = in2 ? 1u << (cur.e2 & 31) : 0u;
-                const uint32_t wlo =
-                    __reduce_or_sync(0xffffffffu, ((cur.e1 & 32) ? 0u : b1) | ((cur.e2 & 32) ? 0u : b2));
-                const uint32_t whi =
-                    __reduce_or_sync(0xffffffffu, ((cur.e1 & 32) ? b1 : 0u) | ((cur.e2 & 32) ? b2 : 0u));
-                const int32_t nc = k < 32 ? __shfl_sync(0xffffffffu, cur.e1, k & 31)
-                                          : (k < 64 ? __shfl_sync(0xffffffffu, cur.e2, k & 31) : cur.e3);
-                if (lane == j) {
-                    cursor += k;
-                    head = nc;
-                    look_ahead();
-                }
-                olo |= wlo;
-                ohi |= whi;
-                m0 |= ((wlo >> lane) & 1u) << j;
-                m1 |= ((whi >> lane) & 1u) << j;
-                if (jn < 0) break;
-                cur = nxt;
-                j = jn;
-            }
-        }
-        const int n_lo = __popc(olo), n_new = n_lo + __popc(ohi);
-        // room in the ring: no producer may still need the slots about to be reused
-        const int need_cons = produced + n_new - kRing;
-        if (need_cons > 0) {
-            const volatile int32_t* cons = R->cons;
-            if (!wait_progress(c, &cons[0], need_cons, &R->done) || !wait_progress(c, &cons[1], need_cons, &R->done))
-                break;
-        }
-        const int base_cell = p * 64;
-        const uint32_t below = (1u << lane) - 1u;
-        if ((olo >> lane) & 1u) {
-            const int u = produced + __popc(olo & below);
-            R->cell[u % kRing] = base_cell + lane;
-            R->mask[u % kRing] = (uint8_t)m0;
-            if (u < kChunk) {
-                R->first_cell[u] = base_cell + lane;
-                R->first_mask[u] = (uint8_t)m0;
-            }
-        }
-        if ((ohi >> lane) & 1u) {
-            const int u = produced + n_lo + __popc(ohi & below);
-            R->cell[u % kRing] = base_cell + 32 + lane;
-            R->mask[u % kRing] = (uint8_t)m1;
-            if (u < kChunk) {
-                R->first_cell[u] = base_cell + 32 + lane;
-                R->first_mask[u] = (uint8_t)m1;
-            }
-        }
-        produced += n_new;
-        __syncwarp();
-        __threadfence_block();
-        if (lane == 0) *reinterpret_cast<volatile int32_t*>(&R->produced) = produced;
-    }
-    __syncwarp();
-    __threadfence_block();
-    if (lane == 0) {
-        *reinterpret_cast<volatile int32_t*>(&R->total) = produced;
-        __threadfence_block();
-        *reinterpret_cast<volatile int32_t*>(&R->done) = 1;
-    }
-}
-
 // ------------------------------------------------------------------ producer
 __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -390,16 +209,6 @@ struct Entries {
     bool exists;   // the chunk exists (a chunk past the end does not)
 };
 
-// The fused path's view of the union: waits until entry `need - 1` is written
-// or the stream is done; returns the union size if it is done, else -1.
-__device__ __forceinline__ bool ring_wait(const Ctx& c, int need, int& total) {
-    UnionRing* R = c.ring;
-    if (!wait_progress(c, &R->produced, need, &R->done)) return false;
-    __threadfence_block();
-    total = *reinterpret_cast<volatile int32_t*>(&R->done) ? *reinterpret_cast<volatile int32_t*>(&R->total) : -1;
-    return true;
-}
-
 // Chunk placement.  `lead` is the index of the first page-aligned union cell
 // after entry 0 among entries 1..63 (0 if there is none).  Chunk c holds union
 // positions p = lead + 64c + slot, slot = 0..63; a position past the end wraps
@@ -409,17 +218,9 @@ __device__ __forceinline__ bool ring_wait(const Ctx& c, int need, int& total) {
 // cells 0-2) followed by whole 64-cell pages, every chunk but the last is one
 // whole page, and each query selects all of such a chunk or none of it.
 __device__ __forceinline__ int union_lead(const Ctx& c, int lane, bool& ok) {
-    int U = c.U;
-    const int32_t* first;
-    if (c.fused) {
-        ok = ring_wait(c, kChunk, U);
-        if (!ok) return 0;
-        U = U < 0 ? kChunk : U;
-        first = c.ring->first_cell;
-    } else {
-        ok = true;
-        first = c.a->union_cells + (size_t)c.g * c.a->union_stride;
-    }
+    const int U = c.U;
+    const int32_t* first = c.ucell;
+    ok = true;
     const uint32_t b0 = __ballot_sync(0xffffffffu, lane >= 1 && lane < U && (first[lane] & (kPage - 1)) == 0);
     if (b0) return __ffs(b0) - 1;
     const uint32_t b1 = __ballot_sync(0xffffffffu, 32 + lane < U && (first[32 + lane] & (kPage - 1)) == 0);
@@ -428,22 +229,8 @@ __device__ __forceinline__ int union_lead(const Ctx& c, int lane, bool& ok) {
 
 __device__ __forceinline__ Entries load_entries(const Ctx& c, int lead, int chunk, int lane, bool& ok) {
     Entries e;
-    int U = c.U;
-    const int32_t* ucell;
-    const uint8_t* umask;
-    bool from_ring = false;
-    if (c.fused) {
-        int total;
-        ok = ring_wait(c, lead + chunk * kChunk + kChunk, total);
-        U = total < 0 ? INT32_MAX : total;   // not done: every position of this chunk is written
-        from_ring = true;
-        ucell = c.ring->cell;
-        umask = c.ring->mask;
-    } else {
-        ok = true;
-        ucell = c.a->union_cells + (size_t)c.g * c.a->union_stride;
-        umask = c.a->union_mask + (size_t)c.g * c.a->union_stride;
-    }
+    const int U = c.U;
+    ok = true;
     e.exists = ok && (long long)chunk * kChunk < (long long)U;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -453,12 +240,9 @@ __device__ __forceinline__ Entries load_entries(const Ctx& c, int lead, int chun
         if (!e.present[k]) {
             e.cell[k] = 0;
             e.mask[k] = 0;
-        } else if (from_ring) {
-            e.cell[k] = u < kChunk ? c.ring->first_cell[u] : ucell[u % kRing];
-            e.mask[k] = u < kChunk ? c.ring->first_mask[u] : umask[u % kRing];
         } else {
-            e.cell[k] = __ldg(ucell + u);
-            e.mask[k] = __ldg(umask + u);
+            e.cell[k] = c.ucell[u];
+            e.mask[k] = c.umask[u];
         }
     }
     return e;
@@ -534,7 +318,6 @@ __device__ void producer_role(const Ctx& c, int first, int lane) {
     s0 = load_scales(c, r0);
     for (int i = first;; i += kStep) {
         const int ts = i % kNS;
-        if (c.fused && lane == 0) *reinterpret_cast<volatile int32_t*>(&c.ring->cons[first]) = lead + (i + 3 * kStep) * kChunk;
         const Entries e3 = load_entries(c, lead, i + 3 * kStep, lane, ok);
         if (!ok) break;
         int pg2[2], r1[2];
@@ -563,8 +346,7 @@ __device__ void producer_role(const Ctx& c, int first, int lane) {
         if (!e0.exists) {   // the stream ended before chunk i: the chunk count is i or i - 1
             if (lane == 0) {
                 T->end = 1;
-                const int U = c.fused ? *reinterpret_cast<volatile int32_t*>(&c.ring->total) : c.U;
-                *c.n_final = (U + kChunk - 1) / kChunk;
+                *c.n_final = (c.U + kChunk - 1) / kChunk;
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(c, BAR_TAB_FULL + ts));
@@ -1064,7 +846,7 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
 }
 
 template <bool kFused>
-__global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(const __grid_constant__ AttnArgs a) {
+__global__ void __launch_bounds__(32 * kWarps, 1) attn_sm_kernel(const __grid_constant__ AttnArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u = smem_u32(smem_raw);
     const uint32_t base_u = (raw_u + 1023u) & ~1023u;
@@ -1074,8 +856,6 @@ __global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(co
     c.base_u = base_u;
     c.abort_flag = reinterpret_cast<volatile int*>(c.base + kOffMisc + 4);
     c.n_final = reinterpret_cast<volatile int*>(c.base + kOffMisc + 8);
-    c.ring = reinterpret_cast<UnionRing*>(c.base + kOffRing);
-    c.fused = kFused;
     c.g = blockIdx.x;
     c.h = blockIdx.y;
     c.q_begin = c.g * kGroup;
@@ -1090,9 +870,9 @@ __global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(co
             if (tid == 0) report(a.dev_status, QSA_DEV_BAD_UNION_COUNT);
             U = U < 0 ? 0 : a.union_stride;
         }
+        c.ucell = a.union_cells + (size_t)c.g * a.union_stride;
+        c.umask = a.union_mask + (size_t)c.g * a.union_stride;
     }
-    c.U = U;
-    c.n_chunks = (U + kChunk - 1) / kChunk;
 
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(c.base + kOffMisc);
     if (tid == 0) {
@@ -1119,12 +899,6 @@ __global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(co
         tc::mbar_init(bar(c, BAR_DRAIN_S), 1);
         tc::mbar_init(bar(c, BAR_DRAIN_PV), 1);
         *c.abort_flag = 0;
-        *c.n_final = kFused ? INT32_MAX : c.n_chunks;
-        c.ring->produced = 0;
-        c.ring->done = 0;
-        c.ring->total = 0;
-        c.ring->cons[0] = 0;
-        c.ring->cons[1] = 0;
         tc::fence_mbar_init();
     }
     if (warp == kWarpMmaS) {
@@ -1135,6 +909,34 @@ __global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(co
     __syncthreads();
     tc::fence_after_sync();
     c.tmem = *tmem_holder;
+    if (kFused) {
+        // The group's union, built by the whole CTA into shared memory before the
+        // pipeline starts (the same build as the union kernel's, so the same
+        // entries in the same order); its scratch is the tile area and the table
+        // ring, not yet in use.
+        const uint32_t cap = fused_union_capacity(a.sel_stride);
+        int32_t* ucell = reinterpret_cast<int32_t*>(c.base + kOffUnion);
+        uint8_t* umask = c.base + kOffUnion + 4 * cap;
+        uint8_t* small = c.base + kOffRawTab;
+        const UnionScratch sc{reinterpret_cast<uint4*>(c.base + kOffKb), small,
+                              reinterpret_cast<uint16_t*>(small + kUnionPages),
+                              reinterpret_cast<int*>(small + 3 * kUnionPages),
+                              reinterpret_cast<int*>(small + 3 * kUnionPages) + kGroup,
+                              reinterpret_cast<int*>(small + 3 * kUnionPages) + 2 * kGroup,
+                              reinterpret_cast<int*>(small + 3 * kUnionPages) + 3 * kGroup,
+                              reinterpret_cast<int*>(small + 3 * kUnionPages) + 4 * kGroup,
+                              reinterpret_cast<int*>(small + 3 * kUnionPages) + 5 * kGroup};
+        // every list holds at most sel_stride cells, so the union fits cap entries
+        U = min(build_group_union<32 * kWarps>(a.sel, a.sel_count, a.n_q, a.sel_stride, c.q_begin, ucell, umask,
+                                               (int)cap, a.dev_status, sc),
+                (int)cap);
+        c.ucell = ucell;
+        c.umask = umask;
+    }
+    c.U = U;
+    c.n_chunks = (U + kChunk - 1) / kChunk;
+    if (tid == 0) *c.n_final = c.n_chunks;
+    __syncthreads();
 
     if (warp == kWarpProducer0 || warp == kWarpProducer1) {
         producer_role(c, warp == kWarpProducer0 ? 0 : 1, lane);
@@ -1146,8 +948,6 @@ __global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(co
         loader_role<false>(c, 32 * k_loader_index(warp) + lane);
     } else if (warp == 20 || warp == 21 || warp == 11 || warp == 15) {
         loader_role<true>(c, 32 * v_loader_index(warp) + lane);
-    } else if (warp == kWarpUnion) {
-        if (kFused) union_role(c, lane);
     } else {
         softmax_role(c, warp >> 3, (warp >> 2) & 1, warp & 3, lane);
     }
@@ -1160,18 +960,23 @@ __global__ void __launch_bounds__(32 * num_warps<kFused>(), 1) attn_sm_kernel(co
 }
 
 template <bool kFused>
-cudaError_t launch_sm(const AttnArgs& a, cudaStream_t stream) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_sm_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+cudaError_t launch_sm(const AttnArgs& a, size_t smem, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(attn_sm_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((a.n_q + kGroup - 1) / kGroup, a.n_kv);
-    attn_sm_kernel<kFused><<<grid, 32 * num_warps<kFused>(), kSmemBytes, stream>>>(a);
+    attn_sm_kernel<kFused><<<grid, 32 * kWarps, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_sm(const AttnArgs& a, cudaStream_t stream) { return launch_sm<false>(a, stream); }
-cudaError_t launch_attn_fused(const AttnArgs& a, cudaStream_t stream) { return launch_sm<true>(a, stream); }
+size_t attn_fused_smem_bytes(int sel_stride) {
+    return (size_t)kSmemBytes + 16 + (size_t)fused_union_capacity(sel_stride) * 5;
+}
+
+cudaError_t launch_attn_sm(const AttnArgs& a, cudaStream_t stream) { return launch_sm<false>(a, kSmemBytes, stream); }
+cudaError_t launch_attn_fused(const AttnArgs& a, cudaStream_t stream) {
+    return launch_sm<true>(a, attn_fused_smem_bytes(a.sel_stride), stream);
+}
 
 }  // namespace qsa

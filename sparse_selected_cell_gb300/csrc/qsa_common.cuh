@@ -123,6 +123,8 @@ struct AttnArgs {
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_sm(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_fused(const AttnArgs& a, cudaStream_t stream);
+// Dynamic shared memory of the fused kernel for lists of sel_stride entries.
+size_t attn_fused_smem_bytes(int sel_stride);
 
 // Per-position attention (no union): each query over its own selection list,
 // with one shared page table (prompt) or one table per query (decode).

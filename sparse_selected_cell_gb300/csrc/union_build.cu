@@ -7,223 +7,32 @@
 // and section "What changed" (one work-group per 8 positions over a local cell
 // bitmap).  Section Extra Notes fixes the storage: int32 cell + separate mask byte.
 //
-// GB300 design: one 512-thread CTA per group.  The group's cell range is walked
-// in windows of kWindow cells held as a byte map in shared memory (byte = the
-// 8-position mask); a context up to kWindow cells is one window.  Each list is
-// sorted, so its cells inside a window form one contiguous index range (found
-// by binary search only when there are several windows).  Two warps mark each
-// list, eight loads in flight per lane before their ORs of bit j into the
-// cell's byte (OR is order-independent, so the result is deterministic).  The
-// window is then compacted in cell order, visiting only the 64-cell pages that
-// hold a marked cell (a page flag is set while marking; the flagged pages are
-// listed in order by one block scan): each warp counts the entries of its
-// contiguous run of listed pages, one shared-memory pass over the warp totals
-// gives each warp its output offset, and each warp writes its pages' entries
-// with warp-level prefix sums, two cells per lane.  Output is sorted by
-// construction and bit-exact.
-#include "qsa_common.cuh"
+// GB300 design: one 512-thread CTA per group, running the shared-memory build of
+// union_core.cuh (a byte map per window of cells, marking, a page scan and an
+// ordered compaction) with its output in the group's rows of the union arrays.
+#include "union_core.cuh"
 
 namespace qsa {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kMarkUnroll = 8;                 // list entries loaded per thread before marking
-constexpr int kWindow = 65536;                 // cells (= bytes of shared memory) per window
-
-__device__ __forceinline__ int lower_bound(const int32_t* __restrict__ a, int n, long long x) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        int mid = (lo + hi) >> 1;
-        if ((long long)__ldg(a + mid) < x) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
-constexpr int kPages = kWindow / kPage;        // 64-cell pages of a window
 
 __global__ void __launch_bounds__(kThreads)
 union_build_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ sel_count, int n_q,
                    int sel_stride, int32_t* __restrict__ ucell, uint8_t* __restrict__ umask,
                    int32_t* __restrict__ ucount, int ustride, int32_t* dev_status) {
-    extern __shared__ uint4 smem_map[];                  // kWindow bytes
-    uint32_t* map32 = reinterpret_cast<uint32_t*>(smem_map);
-    const uint16_t* map16 = reinterpret_cast<const uint16_t*>(smem_map);
-    __shared__ uint8_t s_touched[kPages];                // page p of the window holds a marked cell
-    __shared__ uint16_t s_pages[kPages];                 // the touched pages, in increasing order
-    __shared__ int s_cnt[kGroup];
-    __shared__ int s_first[kGroup], s_last[kGroup];
-    __shared__ int s_beg[kGroup], s_end[kGroup];
+    extern __shared__ uint4 smem_map[];                  // kUnionWindow bytes
+    __shared__ uint8_t s_touched[kUnionPages];
+    __shared__ uint16_t s_pages[kUnionPages];
+    __shared__ int s_small[5 * kGroup];
     __shared__ int s_warp[kThreads / 32];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const UnionScratch sc{smem_map, s_touched, s_pages, s_small, s_small + kGroup, s_small + 2 * kGroup,
+                          s_small + 3 * kGroup, s_small + 4 * kGroup, s_warp};
     const int g = blockIdx.x;
-    const int q_begin = g * kGroup;
-    const int nj = min(kGroup, n_q - q_begin);
     const size_t out_base = (size_t)g * ustride;
-
-    if (tid < kGroup) {
-        int c = 0, first = INT32_MAX, last = INT32_MIN;
-        if (tid < nj) {
-            c = __ldg(sel_count + q_begin + tid);
-            if (c < 0 || c > sel_stride) {
-                report(dev_status, QSA_DEV_BAD_SEL_COUNT);
-                c = c < 0 ? 0 : sel_stride;
-            }
-            if (c > 0) {
-                const int32_t* lst = sel + (size_t)(q_begin + tid) * sel_stride;
-                first = __ldg(lst);
-                last = __ldg(lst + c - 1);
-            }
-        }
-        s_cnt[tid] = c;
-        s_first[tid] = first;
-        s_last[tid] = last;
-    }
-    __syncthreads();
-    long long lo = INT32_MAX, hi = INT32_MIN;
-#pragma unroll
-    for (int j = 0; j < kGroup; ++j) {
-        if (s_cnt[j] > 0) {
-            lo = min(lo, (long long)s_first[j]);
-            hi = max(hi, (long long)s_last[j]);
-        }
-    }
-    int written = 0;   // union entries produced so far (same value in every thread)
-    for (long long w0 = lo & ~(long long)(kPage - 1); w0 <= hi; w0 += kWindow) {
-        // 1. clear the byte map and the page flags of this window (the part it can use)
-        const long long span = min((long long)kWindow, hi - w0 + 1);
-        const int n_pg = (int)((span + kPage - 1) / kPage);   // pages the compaction may read
-        const int n_pieces = n_pg * (kPage / 16);
-        for (int p = tid; p < n_pieces; p += kThreads) smem_map[p] = make_uint4(0, 0, 0, 0);
-        for (int p = tid; p < n_pg; p += kThreads) s_touched[p] = 0;
-        // 2. index range of each list inside [w0, w0 + kWindow)
-        const bool one_window = hi - w0 < kWindow;
-        if (tid < kGroup) {
-            int b = 0, e = 0;
-            if (s_cnt[tid] > 0) {
-                if (one_window) {
-                    e = s_cnt[tid];
-                } else {
-                    const int32_t* lst = sel + (size_t)(q_begin + tid) * sel_stride;
-                    b = lower_bound(lst, s_cnt[tid], w0);
-                    e = lower_bound(lst, s_cnt[tid], w0 + kWindow);
-                }
-            }
-            s_beg[tid] = b;
-            s_end[tid] = e;
-        }
-        __syncthreads();
-        // 3. mark: bit j of the byte of every cell in list j, and the cell's page
-        // flag.  Warps w and w + 8 take list w % 8, kMarkUnroll loads per lane in
-        // flight before the ORs.  Cells outside the window (several windows) or
-        // outside [0, n) cannot occur in one window: lo and hi bound every list.
-        {
-            const int j = warp & (kGroup - 1);
-            if (j < nj) {
-                const int32_t* lst = sel + (size_t)(q_begin + j) * sel_stride;
-                const int e = s_end[j];
-                constexpr int kStride = (kThreads / 32 / kGroup) * 32;   // lanes on one list
-                for (int t0 = s_beg[j] + (warp / kGroup) * 32 + lane; t0 < e; t0 += kStride * kMarkUnroll) {
-                    int cell[kMarkUnroll];
-#pragma unroll
-                    for (int u = 0; u < kMarkUnroll; ++u) {
-                        const int t = t0 + u * kStride;
-                        cell[u] = t < e ? __ldg(lst + t) : INT32_MIN;
-                    }
-#pragma unroll
-                    for (int u = 0; u < kMarkUnroll; ++u) {
-                        const long long off = (long long)cell[u] - w0;
-                        if (cell[u] != INT32_MIN && off >= 0 && off < span) {
-                            atomicOr(map32 + (off >> 2), 1u << (((int)off & 3) * 8 + j));
-                            s_touched[off >> 6] = 1;
-                        }
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        // 4. the touched pages in increasing order: thread t owns flags [2t, 2t+2)
-        {
-            int f[2], c = 0;
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-                const int p = 2 * tid + k;
-                f[k] = p < n_pg ? s_touched[p] : 0;
-                c += f[k];
-            }
-            int incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) s_warp[warp] = incl;
-            __syncthreads();
-            int base = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; ++w) base += w < warp ? s_warp[w] : 0;
-            int idx = base + incl - c;
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                if (f[k]) s_pages[idx++] = (uint16_t)(2 * tid + k);
-        }
-        int n_touched = 0;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) n_touched += s_warp[w];
-        __syncthreads();
-        // 5. compact the touched pages in cell order.  Warp w owns the contiguous
-        // run of touched pages [w * per_warp, (w + 1) * per_warp); a page is one
-        // step of the warp, lane i holding cells 2i and 2i+1.  The warps' entry
-        // counts go through one block pass, then each warp writes its pages with
-        // warp-level scans.
-        const int per_warp = (n_touched + kThreads / 32 - 1) / (kThreads / 32);
-        const int t_lo = min(n_touched, warp * per_warp), t_hi = min(n_touched, t_lo + per_warp);
-        int cnt_w = 0;
-        for (int t = t_lo; t < t_hi; ++t) {
-            const uint32_t two = map16[s_pages[t] * (kPage / 2) + lane];
-            cnt_w += __popc(__ballot_sync(0xffffffffu, (two & 0xFFu) != 0)) +
-                     __popc(__ballot_sync(0xffffffffu, (two >> 8) != 0));
-        }
-        if (lane == 0) s_warp[warp] = cnt_w;
-        __syncthreads();
-        int run = written, total = 0;   // run: output index of this warp's first entry
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) {
-            const int x = s_warp[w];
-            run += w < warp ? x : 0;
-            total += x;
-        }
-        for (int t = t_lo; t < t_hi; ++t) {
-            const int pg = s_pages[t];
-            const uint32_t two = map16[pg * (kPage / 2) + lane];
-            const uint32_t m0 = two & 0xFFu, m1 = two >> 8;
-            const int n = (m0 != 0) + (m1 != 0);
-            int incl = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            int idx = run + incl - n;
-            const int cell0 = (int)(w0 + (long long)pg * kPage) + 2 * lane;
-            if (m0) {
-                if (idx < ustride) {
-                    ucell[out_base + idx] = cell0;
-                    umask[out_base + idx] = (uint8_t)m0;
-                }
-                ++idx;
-            }
-            if (m1 && idx < ustride) {
-                ucell[out_base + idx] = cell0 + 1;
-                umask[out_base + idx] = (uint8_t)m1;
-            }
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        written += total;
-        __syncthreads();      // the map, the page list and s_warp are reused by the next window
-    }
-    if (tid == 0) {
+    int written = build_group_union<kThreads>(sel, sel_count, n_q, sel_stride, g * kGroup, ucell + out_base,
+                                              umask + out_base, ustride, dev_status, sc);
+    if (threadIdx.x == 0) {
         if (written > ustride) {
             report(dev_status, QSA_DEV_UNION_OVERFLOW);
             written = ustride;
@@ -238,10 +47,10 @@ cudaError_t launch_union_build(const int32_t* sel, const int32_t* sel_count, int
                                int32_t* union_cells, uint8_t* union_mask, int32_t* union_count,
                                int union_stride, int32_t* dev_status, cudaStream_t stream) {
     // Per-call (and so per-device) opt-in to the 64 KB byte map.
-    cudaError_t e = cudaFuncSetAttribute(union_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWindow);
+    cudaError_t e = cudaFuncSetAttribute(union_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUnionWindow);
     if (e != cudaSuccess) return e;
     const int n_groups = (n_q + kGroup - 1) / kGroup;
-    union_build_kernel<<<n_groups, kThreads, kWindow, stream>>>(sel, sel_count, n_q, sel_stride, union_cells,
+    union_build_kernel<<<n_groups, kThreads, kUnionWindow, stream>>>(sel, sel_count, n_q, sel_stride, union_cells,
                                                                  union_mask, union_count, union_stride,
                                                                  dev_status);
     return cudaGetLastError();
