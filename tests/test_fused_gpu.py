@@ -5,8 +5,9 @@ attention variant, whose arithmetic it shares -- the output must agree bit for
 bit: the union builder hands the attention pipeline the same chunks in the same
 order.  Against the FP64 oracle it must meet the usual tolerance (max |err| <=
 1e-2 * max|ref|, mean |err| <= 1e-3 * max|ref|): configs 1-3 in full, configs 4-5
-(full size) on sampled positions.  Config 5's unions (~8,000 cells) run through
-the builder's 1,024-entry ring several times.
+(full size) on sampled positions.  Each CTA builds its group's union in shared
+memory with the union kernel's own build before its pipeline starts; config 5's
+unions hold ~8,000 cells each.
 """
 import numpy as np
 import pytest
