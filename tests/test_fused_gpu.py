@@ -2,7 +2,7 @@
 
 Against the launch pair it replaces -- qsa_prompt_attn with the one-CTA-per-SM
 attention variant, whose arithmetic it shares -- the output must agree bit for
-bit: the union builder hands the attention pipeline the same chunks in the same
+bit: the in-CTA union build hands the attention pipeline the same chunks in the same
 order.  Against the FP64 oracle it must meet the usual tolerance (max |err| <=
 1e-2 * max|ref|, mean |err| <= 1e-3 * max|ref|): configs 1-3 in full, configs 4-5
 (full size) on sampled positions.  Each CTA builds its group's union in shared
@@ -142,9 +142,8 @@ def test_fused_bad_counts_are_clamped_and_reported(qsa):
 def test_fused_mixed_whole_and_partial_pages(qsa):
     """Lists that mix whole pages with pages they hold only in part, at every
     density, several lists sharing a page while holding different parts of it, up
-    to the 2,051-cell cap: the union builder's whole-page checks (all lists at
-    once) and its batched reads of partly held pages, against the launch pair bit
-    for bit and against the oracle."""
+    to the 2,051-cell cap (many partly held pages in the in-CTA union build),
+    against the launch pair bit for bit and against the oracle."""
     w = gen.make(2, n_q=64)          # 4,096-cell context: pages 0-63
     rng = np.random.default_rng(23)
     shared = sorted(rng.choice(64, size=20, replace=False).tolist())   # pages several lists touch
