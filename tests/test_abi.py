@@ -110,3 +110,5 @@ def test_fused_host_argument_checks(lib):
     assert fused(sel=None) == ERR_ARG
     assert fused(cnt=None) == ERR_ARG
     assert fused(n_kv=0) == ERR_ARG
+    # the union of 8 lists of 4,000 entries would not fit a CTA's shared memory
+    assert fused(sel_stride=4000) == 2   # QSA_ERR_UNSUPPORTED
