@@ -159,7 +159,8 @@ int qsa_prompt_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_poo
  *   - The union of 8 lists (up to 8 x sel_stride entries, 5 bytes each) must fit
  *     the CTA's shared memory next to the pipeline's (sm_103's per-block limit
  *     of 227 KB): sel_stride up to about 2,800 (2,056 holds the method's
- *     2,051-cell cap); QSA_ERR_UNSUPPORTED, before any CUDA call, above that.
+ *     2,051-cell cap); QSA_ERR_UNSUPPORTED, before any CUDA call, above that,
+ *     and for more than 65,535 groups (n_q > 524,280).
  *   - n_q == 0 returns QSA_OK with no launch. */
 int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool,
                    const uint16_t* k_scale, const uint16_t* v_scale,

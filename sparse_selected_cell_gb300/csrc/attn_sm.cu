@@ -856,8 +856,9 @@ __global__ void __launch_bounds__(32 * kWarps, 1) attn_sm_kernel(const __grid_co
     c.base_u = base_u;
     c.abort_flag = reinterpret_cast<volatile int*>(c.base + kOffMisc + 4);
     c.n_final = reinterpret_cast<volatile int*>(c.base + kOffMisc + 8);
-    c.g = blockIdx.x;
-    c.h = blockIdx.y;
+    // fused path: the KV heads of a group are neighbours in the grid, so its lists are read while L2 holds them
+    c.g = kFused ? blockIdx.y : blockIdx.x;
+    c.h = kFused ? blockIdx.x : blockIdx.y;
     c.q_begin = c.g * kGroup;
     c.nj = min(kGroup, a.n_q - c.q_begin);
     c.n_heads = a.n_kv * kHeadsPerKv;
@@ -963,7 +964,8 @@ template <bool kFused>
 cudaError_t launch_sm(const AttnArgs& a, size_t smem, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(attn_sm_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((a.n_q + kGroup - 1) / kGroup, a.n_kv);
+    const unsigned n_groups = (unsigned)((a.n_q + kGroup - 1) / kGroup);
+    const dim3 grid = kFused ? dim3((unsigned)a.n_kv, n_groups) : dim3(n_groups, (unsigned)a.n_kv);
     attn_sm_kernel<kFused><<<grid, 32 * kWarps, smem, stream>>>(a);
     return cudaGetLastError();
 }

@@ -146,6 +146,8 @@ int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool
     // the group's union (up to 8 x sel_stride entries) must fit the CTA's shared
     // memory next to the pipeline's: sm_103's per-block opt-in limit is 227 KB
     if (qsa::attn_fused_smem_bytes(sel_stride) > (size_t)227 * 1024) return QSA_ERR_UNSUPPORTED;
+    // the fused grid is (KV head, group): the group count is its y extent
+    if ((n_q + qsa::kGroup - 1) / qsa::kGroup > 65535) return QSA_ERR_UNSUPPORTED;
     const qsa::AttnArgs a{q, k_pool, v_pool, k_scale, v_scale, page_table, n_lpages, n_ppages, n_kv,
                           nullptr, nullptr, nullptr, 0, n_q, sm_scale, out, dev_status,
                           sel, sel_count, sel_stride};

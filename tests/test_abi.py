@@ -112,3 +112,4 @@ def test_fused_host_argument_checks(lib):
     assert fused(n_kv=0) == ERR_ARG
     # the union of 8 lists of 4,000 entries would not fit a CTA's shared memory
     assert fused(sel_stride=4000) == 2   # QSA_ERR_UNSUPPORTED
+    assert fused(n_q=8 * 65536) == 2     # more groups than the grid's y extent holds
