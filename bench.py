@@ -129,25 +129,23 @@ def algorithmic(w, union_count):
                 mean_union=float(U.mean()), union_ratio=float(U.mean() / w.sel_count.mean()))
 
 
-def read_traffic(kernel: str, sources):
-    """DRAM bytes per launch for `kernel` from the committed ncu summaries, if the
-    kernel's sources still hash to what the capture recorded; else None."""
+def read_traffic(profile: str, kernel: str, sources):
+    """DRAM bytes per launch from the committed ncu summary profiles/<profile>.txt
+    (one kernel on one workload), if it names `kernel` and the kernel's sources
+    still hash to what the capture recorded; else None.  Returns (bytes, hash)."""
     h = hashlib.sha256()
     for s in sources:
         h.update(open(os.path.join(ROOT, s), "rb").read())
     digest = h.hexdigest()[:16]
-    pdir = os.path.join(ROOT, "profiles")
-    if not os.path.isdir(pdir):
+    path = os.path.join(ROOT, "profiles", profile + ".txt")
+    if not os.path.isfile(path):
         return None, digest
-    for f in sorted(os.listdir(pdir)):
-        if not f.endswith(".txt"):
-            continue
-        txt = open(os.path.join(pdir, f)).read()
-        m_k = re.search(r"^kernel:\s*(\S+)", txt, re.M)
-        m_h = re.search(r"^source_sha256_16:\s*(\S+)", txt, re.M)
-        m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
-        if m_k and m_h and m_t and m_k.group(1) == kernel and m_h.group(1) == digest:
-            return float(m_t.group(1)), digest
+    txt = open(path).read()
+    m_k = re.search(r"^kernel:\s*(\S+)", txt, re.M)
+    m_h = re.search(r"^source_sha256_16:\s*(\S+)", txt, re.M)
+    m_t = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
+    if m_k and m_h and m_t and m_k.group(1) == kernel and m_h.group(1) == digest:
+        return float(m_t.group(1)), digest
     return None, digest
 
 
@@ -341,6 +339,9 @@ def decode_bench(args):
     cells = int((resident & (np.arange(w.sel.shape[1])[None, :] < w.sel_count[:, None])).sum())
     alg = cells * w.n_kv * 260 + w.n_seq * w.n_heads * 128 * 6
     achieved = alg / (ms / 1e3) / 1e9
+    traffic, digest = read_traffic("select_attn_kernel_decode1k-ctx32k", "select_attn_kernel",
+                                   ["sparse_selected_cell_gb300/csrc/select_attn.cu",
+                                    "sparse_selected_cell_gb300/csrc/qsa_common.cuh"])
     print(json.dumps({"mode": "decode", "metric": "decode query-head rows/s", "unit": "query-head rows/s",
                       "value": w.n_seq * w.n_heads / (ms / 1e3), "ms_per_step": ms, "steps": args.steps,
                       "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
@@ -351,7 +352,9 @@ def decode_bench(args):
                       "roofline": {"bound": "hbm", "kernel": "select_attn_kernel", "achieved": achieved, "peak": hbm,
                                    "unit": "GB/s", "frac": achieved / hbm, "peak_source": src,
                                    "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
-                                   "algorithmic_bytes_per_launch": alg},
+                                   "algorithmic_bytes_per_launch": alg, "traffic": traffic,
+                                   "traffic_over_algorithmic": (traffic / alg) if traffic else None,
+                                   "source_sha256_16": digest},
                       "status": int(st.item())}), flush=True)
 
 
@@ -513,13 +516,18 @@ def measure(args, w, dev, world: int, rank: int, headline: bool):
     t_tc = alg["flops"] / (bf16_sus * 1e12) * 1e3
     resolved = args.variant or qsa.default_variant()
     if args.fused:
-        kernel, files, vname = "attn_sm_kernel", ("attn_sm.cu", "tc_ptx.cuh"), "fused (union built in the CTA)"
+        kernel, files, vname = ("attn_sm_kernel", ("attn_sm.cu", "tc_ptx.cuh", "union_core.cuh"),
+                                "fused (union built in the CTA)")
     else:
         kernel, files = {qsa.ATTN_TCGEN05: ("attn_tc_kernel", ("attn_tc.cu", "tc_ptx.cuh")),
                          qsa.ATTN_TCGEN05_SM: ("attn_sm_kernel", ("attn_sm.cu", "tc_ptx.cuh"))}[resolved]
         vname = {1: "tcgen05, two CTAs per SM", 2: "tcgen05, one CTA per SM"}[resolved]
     srcs = ["sparse_selected_cell_gb300/csrc/" + f for f in files + ("qsa_common.cuh",)]
-    traffic, digest = read_traffic(kernel, srcs)
+    # a capture covers one named workload at its full size and drift
+    named = next((c for c in gen.CONFIGS.values() if c["name"] == w.name), None)
+    full = named is not None and w.n_q == named["n_q"] and w.drift == named["drift"]
+    profile = f"{kernel}{'_fused' if args.fused else ''}_{w.name}"
+    traffic, digest = read_traffic(profile, kernel, srcs) if full else (None, None)
     in_bytes = sum(v.numel() * v.element_size() for v in d.values())
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,

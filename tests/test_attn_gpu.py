@@ -256,3 +256,20 @@ def test_query_magnitudes_far_from_one(qsa, variant, shift):
     assert st == 0
     ref = oracle.attn_ref(q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, w.sel, w.sel_count, w.n_kv, sm)
     check_close(got, ref, f"Q x 2^{shift}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_query_rows_scaled_apart(qsa, variant):
+    """Some query heads times 2^20, the rest as they are, sm_scale times 2^-20: the
+    scaled heads keep their scores and the others get nearly equal weights, so
+    rows of one chunk take different power-of-two scalings."""
+    w = gen.make(2, n_q=40, seed=53)
+    big = np.isin(np.arange(w.n_heads) % 12, [1, 4, 9, 10])
+    qf = (w.q.astype(np.uint32) << 16).view(np.float32)
+    qf[:, big] *= np.float32(2.0 ** 20)   # exact
+    q = (qf.view(np.uint32) >> 16).astype(np.uint16)
+    sm = float(2.0 ** -20 / np.sqrt(128.0))
+    got, st = _run_scaled(qsa, w, variant, sm, q=q)
+    assert st == 0
+    ref = oracle.attn_ref(q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, w.sel, w.sel_count, w.n_kv, sm)
+    check_close(got, ref, "rows scaled apart")

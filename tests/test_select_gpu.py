@@ -32,12 +32,12 @@ def check_close(got, ref, what=""):
     assert err.mean() <= 1e-3 * scale, f"{what}: mean err {err.mean():.3e} vs scale {scale:.3f}"
 
 
-def run_sel(qsa, w, **over):
+def run_sel(qsa, w, sm_scale=None, **over):
     d = qsa.to_device(w)
     d.update({k: torch.from_numpy(np.ascontiguousarray(v)).cuda() for k, v in over.items()})
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = qsa.select_attn(d["q"], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"],
-                          d["sel"], d["sel_count"], dev_status=status)
+                          d["sel"], d["sel_count"], sm_scale=sm_scale, dev_status=status)
     torch.cuda.synchronize()
     return out.cpu().numpy(), int(status.item())
 
@@ -106,3 +106,56 @@ def test_select_empty_batch(qsa):
     out = qsa.select_attn(d["q"][:0], d["k_pool"], d["v_pool"], d["k_scale"], d["v_scale"], d["page_table"],
                           d["sel"][:0], d["sel_count"][:0])
     assert out.shape == (0, w.n_heads, 128)
+
+
+def _times_pow2(q_bits, shift):
+    """BF16 bits times 2^shift (exact: only the exponent moves)."""
+    qf = (q_bits.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** shift)
+    return (qf.view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("shift", [20, -20])
+def test_select_query_magnitudes_far_from_one(qsa, shift):
+    """Q times 2^shift with sm_scale times 2^-shift: the same scores.  Rows whose
+    largest |q| is 2^14 or more, or below 2^-10, take the exact power-of-two row
+    scaling of the FP16 score path; the oracle sees the same scaled inputs."""
+    w = gen.make(2, n_q=40, seed=47)
+    q = _times_pow2(w.q, shift)
+    sm = float(2.0 ** -shift / np.sqrt(128.0))
+    got, st = run_sel(qsa, w, sm_scale=sm, q=q)
+    assert st == 0
+    ref = oracle.attn_ref(q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, w.sel, w.sel_count, w.n_kv, sm)
+    check_close(got, ref, f"Q x 2^{shift}")
+
+
+def test_select_query_rows_scaled_apart(qsa):
+    """Some query heads times 2^20, the rest as they are, sm_scale times 2^-20: the
+    scaled heads keep their scores and the others get nearly equal weights.  Rows
+    of one (position, KV head) then take different power-of-two scalings, rows
+    0-7 and 8-11 of the tile among them."""
+    w = gen.make(2, n_q=40, seed=53)
+    big = np.isin(np.arange(w.n_heads) % 12, [1, 4, 9, 10])
+    q = w.q.copy()
+    q[:, big] = _times_pow2(w.q[:, big], 20)
+    sm = float(2.0 ** -20 / np.sqrt(128.0))
+    got, st = run_sel(qsa, w, sm_scale=sm, q=q)
+    assert st == 0
+    ref = oracle.attn_ref(q, w.k_pool, w.v_pool, w.k_scale, w.v_scale, w.page_table, w.sel, w.sel_count, w.n_kv, sm)
+    check_close(got, ref, "rows scaled apart")
+
+
+def test_select_scale_signs_and_ranges(qsa):
+    """K scales of either sign; V scales of either sign and of any FP16 size (zero,
+    subnormal, up to 2^15), which the kernel splits into a power of two, carried in
+    the softmax's exponent, and a significand in P; a non-default sm_scale."""
+    w = gen.make(2, n_q=40, seed=59)
+    rng = np.random.default_rng(7)
+    ks = (w.k_scale * rng.choice([-1.0, 1.0], size=w.k_scale.shape)).astype(np.float16)
+    mag = np.exp2(rng.uniform(-24.0, 15.0, size=w.v_scale.shape))
+    vs = (mag * rng.choice([-1.0, 1.0], size=mag.shape)).astype(np.float16)
+    vs[rng.random(vs.shape) < 0.05] = 0
+    assert (np.abs(vs[vs != 0]) < np.float16(2.0 ** -14)).any()   # FP16 subnormals among them
+    got, st = run_sel(qsa, w, sm_scale=0.05, k_scale=ks.view(np.int16), v_scale=vs.view(np.int16))
+    assert st == 0
+    ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, ks, vs, w.page_table, w.sel, w.sel_count, w.n_kv, 0.05)
+    check_close(got, ref, "scale signs and ranges")
