@@ -12,6 +12,9 @@ the data path).  `roofline` describes the attention kernel (the dominant one).
 `e2e` repeats the measurement through the public call with pinned host buffers,
 host->device inputs and device->host outputs inside the timed region.
 `cpu_baseline` times the FP64 CPU oracle on a bounded sample on the host cores.
+On one GPU the default run also nests `decode`: qsa_decode_attn over 1,024
+sequences of 32,768 cells, one query each (its own workload, its own roofline;
+--no-decode leaves it out, --decode prints it as the only line).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --config N            one of the five workloads (default 4)
@@ -85,6 +88,8 @@ def parse():
                    help="0 default, 1 tcgen05 (two CTAs per SM), 2 tcgen05 (one CTA per SM)")
     p.add_argument("--e2e-steps", type=int, default=50)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-decode", action="store_true",
+                   help="leave out the decode measurement nested in the default line")
     p.add_argument("--decode", action="store_true",
                    help="time decode over a batch of sequences (qsa_decode_attn) instead of the prompt chunk")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
@@ -307,14 +312,20 @@ def drift_sweep(args):
 
 
 def decode_bench(args):
-    """Decode over a batch of sequences (qsa_decode_attn): one query per sequence,
-    each with its own page table into one shared 1 GB pool (far above L2), timed
-    with CUDA events; one JSON line, separate from the prompt-chunk headline."""
+    """`--decode`: the decode measurement below as its own JSON line."""
     import torch
     from sparse_selected_cell_gb300 import build as qbuild
-    from sparse_selected_cell_gb300 import gen, qsa
     torch.cuda.set_device(0)
     qbuild.build()
+    print(json.dumps(decode_measure(args.steps, args.warmup)), flush=True)
+
+
+def decode_measure(steps: int, warmup: int) -> dict:
+    """Decode over a batch of sequences (qsa_decode_attn): one query per sequence,
+    each with its own page table into one shared 1 GB pool (far above L2), timed
+    with CUDA events over `steps` launches after `warmup` untimed ones."""
+    import torch
+    from sparse_selected_cell_gb300 import gen, qsa
     w = gen.make_decode(**gen.DECODE_BENCH)
 
     def dev(x):
@@ -325,15 +336,15 @@ def decode_bench(args):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.empty((w.n_seq, w.n_heads, 128), dtype=torch.float32, device="cuda")
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    for _ in range(args.warmup):
+    for _ in range(max(3, warmup)):
         qsa.decode_attn(q, kp, vp, ks, vs, pts, sel, cnt, out=out, dev_status=st)
     torch.cuda.synchronize()
     ev[0].record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         qsa.decode_attn(q, kp, vp, ks, vs, pts, sel, cnt, out=out, dev_status=st)
     ev[1].record()
     torch.cuda.synchronize()
-    ms = ev[0].elapsed_time(ev[1]) / args.steps
+    ms = ev[0].elapsed_time(ev[1]) / steps
     hbm, _, _, src = peaks()
     resident = w.page_tables[np.arange(w.n_seq)[:, None], np.where(w.sel >= 0, w.sel >> 6, 0)] >= 0
     cells = int((resident & (np.arange(w.sel.shape[1])[None, :] < w.sel_count[:, None])).sum())
@@ -342,9 +353,9 @@ def decode_bench(args):
     traffic, digest = read_traffic("select_attn_kernel_decode1k-ctx32k", "select_attn_kernel",
                                    ["sparse_selected_cell_gb300/csrc/select_attn.cu",
                                     "sparse_selected_cell_gb300/csrc/qsa_common.cuh"])
-    print(json.dumps({"mode": "decode", "metric": "decode query-head rows/s", "unit": "query-head rows/s",
-                      "value": w.n_seq * w.n_heads / (ms / 1e3), "ms_per_step": ms, "steps": args.steps,
-                      "warmup": args.warmup, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+    return dict({"mode": "decode", "metric": "decode query-head rows/s", "unit": "query-head rows/s",
+                      "value": w.n_seq * w.n_heads / (ms / 1e3), "ms_per_step": ms, "steps": steps,
+                      "warmup": max(3, warmup), "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
                       "config": {"workload": f"decode: {w.n_seq:,} sequences x {w.ctx:,} cells, {w.n_kv} KV heads "
                                              f"x 12, one query per sequence, page tables into a shared pool of "
                                              f"{w.n_ppages:,} pages", "l2": "pool of %.2f GB, above L2"
@@ -355,7 +366,7 @@ def decode_bench(args):
                                    "algorithmic_bytes_per_launch": alg, "traffic": traffic,
                                    "traffic_over_algorithmic": (traffic / alg) if traffic else None,
                                    "source_sha256_16": digest},
-                      "status": int(st.item())}), flush=True)
+                      "status": int(st.item())})
 
 
 def custom_config(args, rank: int):
@@ -608,10 +619,15 @@ def main():
         jobs = [(gen.make(cfg, seed=rank_seed(rank, cfg), n_q=args.n_q), True)]
     for w, headline in jobs:
         line = measure(args, w, dev, world, rank, headline)
-        if line is not None:
-            print(json.dumps(line), flush=True)
         del w
         torch.cuda.empty_cache()
+        if line is not None and headline and world == 1 and not (args.no_decode or args.fused) and args.context is None \
+                and args.config == CONFIG_ID and args.n_q is None and not args.all_configs:
+            # the decode path on its own workload, nested in the same line (one line per run)
+            line["decode"] = decode_measure(min(args.steps, 100), args.warmup)
+            torch.cuda.empty_cache()
+        if line is not None:
+            print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
 
