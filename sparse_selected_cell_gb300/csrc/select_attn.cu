@@ -24,15 +24,15 @@
 //     page-table entries of step t+2 are loaded, and step t+1's K and V rows
 //     are copied with 16-byte cp.async into a 2-deep INT8 stage ring, 16-byte
 //     chunks XOR-swizzled by cell).  The two lanes copy the two halves of each
-//     32-byte sector in the same instruction, so L2 serves every sector once
-//     (one lane per row, 16 bytes at a time, asked for each sector twice); the
-//     rows' K/V scales are loaded with the copies and stored a step later, so
-//     no step waits on them;
+//     32-byte sector in the same instruction (with one lane per row, the halves
+//     came from two instructions); the rows' K/V scales are loaded with the
+//     copies and stored a step later, so no step waits on them;
 //   * S = Q K^T with mma.sync m16n8k16 on FP16 operands (Q converted from BF16
-//     when the CTA stores it, which is exact inside FP16's range, as in the
-//     union kernel): each lane's K operand is one 32-bit word of the INT8 row
-//     (the head dimension is permuted inside every 16-wide k step, for Q and K
-//     alike), converted exactly in registers (|int8| <= 128 fits FP16); the K scale (times sm_scale and log2 e)
+//     once per CTA, exactly: rows far from FP16's range take a power-of-two
+//     scaling, as in the union kernel): each lane's K operand is one 32-bit word
+//     of the INT8 row (the head dimension is permuted inside every 16-wide k
+//     step, for Q and K alike), converted exactly in registers (|int8| <= 128
+//     fits FP16); the K scale (times sm_scale and log2 e)
 //     multiplies each score column in FP32, unselected / masked cells are -inf,
 //     the online softmax runs in the exp2 domain with the same lazy rescale as
 //     the union kernel, and P = p * (V scale) enters O += P V as BF16; V also
