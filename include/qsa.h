@@ -78,9 +78,10 @@ enum {
     QSA_ATTN_DEFAULT = 0,
     QSA_ATTN_TCGEN05 = 1,   /* tcgen05.mma with TMEM accumulators, warp-specialised pipeline,
                                one CTA per (group, KV head), 64-cell chunks, two CTAs per SM */
-    QSA_ATTN_TCGEN05_SM = 2 /* tcgen05, one CTA per (group, KV head) and per SM: Q, O and four
-                               S/P buffers in TMEM, two softmax warp sets on alternating chunks
-                               (the kernel qsa_fused_attn runs with the union built in-CTA) */
+    QSA_ATTN_TCGEN05_SM = 2 /* tcgen05, one CTA per (group, KV head) and per SM: Q, an O per
+                               softmax set and three S/P buffers in TMEM, two softmax warp sets
+                               on alternating chunks, combined at the end (the kernel
+                               qsa_fused_attn runs with the union built in-CTA) */
 };
 
 /* The variant QSA_ATTN_DEFAULT resolves to in this build (one of the values above). */
@@ -174,9 +175,11 @@ int qsa_fused_attn(const uint16_t* q, const int8_t* k_pool, const int8_t* v_pool
  * selection unions on XMX", Strata PR #2808, section Summary: the prompt path's
  * default, each position gathering its own ~2,051 cells; section Extra Notes
  * times it against the union kernel).  It is the baseline the union path
- * replaces, built on the warp-level tensor path (mma.sync, BF16 in, FP32 sums)
- * with the union kernels' K/V handling in BF16: exact BF16 K and V, K scale on
- * the score column in FP32, V scale in P.  Each (query, KV head) list is split
+ * replaces, built on the warp-level tensor path (mma.sync, FP32 sums): S on FP16
+ * operands (Q converted from BF16 with the union kernel's exact power-of-two row
+ * scaling, K as the exact INT8 integers, its scale on the score column in FP32),
+ * P V on BF16 operands (V exact, P = p * v_scale rounded to BF16 once).  Each
+ * (query, KV head) list is split
  * over four warps whose partial softmax states are merged at the end, so the
  * summation order differs from a single walk of the list (results agree within
  * BF16 rounding of the weights).  Arguments and layouts are those of

@@ -1,5 +1,6 @@
-// attn_sm.cu -- union attention with one CTA per SM: Q, O and four S/P
-// buffers in Tensor Memory, two softmax warp sets on alternating chunks; and
+// attn_sm.cu -- union attention with one CTA per SM: Q, an O per softmax set
+// and three S/P buffers in Tensor Memory, two softmax warp sets on alternating
+// chunks, each with its own running max, combined at the end; and
 // the same kernel with the group's union built inside the CTA (the fused path,
 // no union arrays in global memory and no first launch).
 //
@@ -15,22 +16,23 @@
 //
 // One CTA per (group g, KV head h) on its own SM: 96 query-head rows (row r =
 // j*12 + hq, TMEM lane r).  The CTA owns all 512 TMEM columns: Q [0,64) as FP16
-// pairs (the A operand of S), O [64,192), and four S/P buffers of 64 columns
-// from 192, so S can run up to three chunks ahead of the softmax.  Warp roles:
+// pairs (the A operand of S), set 0's O [64,192), set 1's O [192,320), and three
+// S/P buffers of 64 columns from 320, so S can run up to two chunks ahead of the
+// softmax.  Warp roles:
 //   softmax, two sets of six: set s (warps 8s + {0,1,2,4,5,6}) takes the chunks
 //              t with t % 2 == s.  Within a set, warps 8s+q and 8s+q+4 own the
 //              32 rows of TMEM lane quadrant q and columns [0,32) / [32,64) of
 //              the chunk and swap half-chunk maxima (a 64-thread named
 //              barrier).  A warp reads its 32 S columns, scales each by its K
-//              scale, masks cells its query did not select, and takes the
-//              running max m of chunk t-1 from the other set (a shared-memory
-//              slot per row and an mbarrier): m only moves when a weight would
-//              exceed 2^12 (lazy rescale), so the two sets' chunks overlap and
-//              only this scalar passes between them.  It writes P = p * (V
-//              scale) as FP16 over its own S columns and keeps its own FP32 sum
-//              of p, relative to the m it last used.  At the end the four warps
-//              of a quadrant bring their sums to the final m, add them, and
-//              each stores 32 of O's columns.  Set 0 writes Q into TMEM first.
+//              scale and masks cells its query did not select.  Each set keeps
+//              its own running max m (it only moves when a weight would exceed
+//              2^12: lazy rescale), its own O (P(t) V accumulates into the O of
+//              the set that took chunk t) and per warp its FP32 sum of p, so
+//              the sets never wait for each other.  A warp writes P = p * (V
+//              scale) as FP16 over its own S columns.  At the end the four warps
+//              of a quadrant take M = max(m_0, m_1), weigh each set's sums and O
+//              by 2^(m_s - M), and each stores 32 of the output's columns.  Set 0
+//              writes Q into TMEM first.
 //   warps 3, 22 producers (even / odd chunks): union entries -> page table ->
 //              per-chunk tables in a 16-deep ring (pool row of each cell, K scale
 //              times sm_scale * log2(e), V scale divided by a power of two per
@@ -40,8 +42,9 @@
 //              writes one end-of-stream table.
 //   warps 7, 23 MMA issuers (the whole warp runs the loop; one elected lane
 //              issues): warp 7 S(t) = Q K^T (A = Q from TMEM, B = K tile, M=128
-//              N=64 K=128) into S buffer t % 4, warp 23 O += P(t) V (A = P from
-//              TMEM, B = V tile, M=128 N=128 K=64), all operands FP16.
+//              N=64 K=128) into S buffer t % 3, warp 23 O += P(t) V (A = P from
+//              TMEM, B = V tile, M=128 N=128 K=64) into the O of chunk t's set, all
+//              operands FP16.
 //   warps 16-19 K loaders, warps 11, 15, 20, 21 V loaders: one 16-byte load per
 //              row and thread of the chunk's INT8 rows, issued two chunks ahead
 //              into registers, converted exactly to FP16 straight into operand
@@ -77,11 +80,11 @@ constexpr int kWarpMmaS = 7, kWarpMmaPV = 23;             // S issuer, P V issue
 constexpr int kLoadThreads = 128;            // per loader group (K or V)
 constexpr int kSetWarps = 6;                 // softmax warps per set
 constexpr int kNS = 16;                      // per-chunk table ring
-constexpr int kNSb = 4;                      // S/P buffers in TMEM
+constexpr int kNSb = 3;                      // S/P buffers in TMEM
 constexpr int kNK = 3;                       // K tiles
 constexpr int kNV = 3;                       // V tiles
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0, kColO = 64, kColS = 192;   // S buffer b at kColS + 64 b
+constexpr uint32_t kColQ = 0, kColO = 64, kColS = 320;   // O of set s at kColO + 128 s; S buffer b at kColS + 64 b
 // Lazy rescale threshold (exp2 domain): the running max only moves, and O is
 // only rescaled, when a weight exceeds it by more than 2^12.  P = e * vs' then
 // stays below 2^13, inside FP16, and FP16 / FP32 rounding is relative, so a
@@ -112,26 +115,27 @@ constexpr uint32_t kOffKb = 0;
 constexpr uint32_t kOffVb = kOffKb + kNK * kTileBytes;
 constexpr uint32_t kOffRawTab = kOffVb + kNV * kTileBytes;
 // Shared scalars per row: half-chunk maxima swapped within a set, by set and
-// chunk parity [2][2][2][96]; the running max handed between sets [2][96]; the
-// row sums at the end [4][96]; the Q row scale [96].
+// chunk parity [2][2][2][96]; each set's final running max [2][96]; the row sums
+// at the end [4][96]; the Q row scale [96].
 constexpr uint32_t kOffXchg = kOffRawTab + kNS * (uint32_t)sizeof(RawTab);
 constexpr uint32_t kOffMslot = kOffXchg + 8 * kRows * 4;
 constexpr uint32_t kOffLsum = kOffMslot + 2 * kRows * 4;
 constexpr uint32_t kOffRs = kOffLsum + 4 * kRows * 4;
 constexpr uint32_t kOffBars = (kOffRs + kRows * 4 + 7u) & ~7u;
-// K_EMPTY[b]: S(t) with t % kNK == b has read K tile b.  S_FULL[b]: S(t), t % 4
+// K_EMPTY[b]: S(t) with t % kNK == b has read K tile b.  S_FULL[b]: S(t), t % 3
 // == b, is in S buffer b.  P_READY[b]: P(t) is in S buffer b (or, at t = the
 // chunk count, the stream has ended).  V_EMPTY[b]: P(t) V with t % kNV == b
-// has completed (V tile b free).  PV_DONE[b]: P(t) V with t % 4 == b has
-// completed, so O holds every P V up to chunk t.  The softmax warp of chunk t
-// waits on it for P(t-1) V: it has seen S(t) complete, and S(t) was issued
-// after P(t-4) V had completed, so the slot's previous phase (P(t-5) V) is
-// complete and a parity wait cannot mistake it for the one it wants.
-// M_READY[b]: the set that took chunk t, t % 2 == b, has published its m.
+// has completed (V tile b free).  PV_DONE[b]: P(t) V with t % 3 == b has
+// completed.  Before it rescales its set's O, the softmax warp of chunk t waits
+// on it for P(t-2) V, the set's previous chunk (P V runs in chunk order, so
+// every earlier P V into that O is complete too).  The slot cannot be a phase
+// further on: P(t+1) V follows P(t) V, which needs this warp's P(t).  And its
+// previous phase (P(t-5) V) is complete: the warp has seen S(t) complete, issued
+// after P(t-3) V had completed.
 enum { BAR_TAB_FULL = 0, BAR_TAB_EMPTY = kNS, BAR_K_FULL = 2 * kNS, BAR_K_EMPTY = BAR_K_FULL + kNK,
        BAR_V_FULL = BAR_K_EMPTY + kNK, BAR_V_EMPTY = BAR_V_FULL + kNV, BAR_S_FULL = BAR_V_EMPTY + kNV,
-       BAR_P_READY = BAR_S_FULL + kNSb, BAR_PV_DONE = BAR_P_READY + kNSb, BAR_M_READY = BAR_PV_DONE + kNSb,
-       BAR_O_DONE = BAR_M_READY + 2, BAR_Q_READY, BAR_DRAIN_S, BAR_DRAIN_PV, NUM_BARS };
+       BAR_P_READY = BAR_S_FULL + kNSb, BAR_PV_DONE = BAR_P_READY + kNSb, BAR_O_DONE = BAR_PV_DONE + kNSb,
+       BAR_Q_READY, BAR_DRAIN_S, BAR_DRAIN_PV, NUM_BARS };
 constexpr uint32_t kOffMisc = kOffBars + NUM_BARS * 8;      // tmem base, abort flag, chunk count
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;           // + alignment slack
@@ -488,8 +492,8 @@ __device__ void loader_role(const Ctx& c, int ct) {
 // ------------------------------------------------------------------ MMA issuers
 // Two warps issue (the whole warp runs the loop, one elected lane issues), so
 // the waits of one stream do not hold up the other.  The S issuer: S(t) needs
-// chunk t's K tile and S buffer t % 4 back, i.e. P(t-4) V complete (it read
-// P(t-4) from that buffer).  The P V issuer: P(t) V needs P(t) and chunk t's V
+// chunk t's K tile and S buffer t % 3 back, i.e. P(t-3) V complete (it read
+// P(t-3) from that buffer).  The P V issuer: P(t) V needs P(t) and chunk t's V
 // tile; tcgen05.mma from one thread executes in issue order, so the P V stream
 // accumulates into O in chunk order.  Both learn the chunk count from the
 // stream's end (an extra K_FULL arrival; P_READY of the chunk past the last).
@@ -527,8 +531,8 @@ __device__ void mma_s_role(const Ctx& c) {
 __device__ void mma_pv_role(const Ctx& c) {
     constexpr uint32_t idO = tc::idesc_bf16(128, kHeadDim, false, true) & kF16;  // A = P (TMEM), B = V tile, MN-major
     const uint64_t dv0 = tc::smem_desc(c.base_u + kOffVb, 8192, 1024, 2);
-    const uint32_t tO = c.tmem + kColO;
     for (int t = 0;; ++t) {
+        const uint32_t tO = c.tmem + kColO + 128 * (t & 1);   // the O of the set that took chunk t
         const int b = t % kNV, sb = t % kNSb;
         if (!wait_addr(c, bar(c, BAR_P_READY + sb), (t / kNSb) & 1)) break;
         if (t >= *c.n_final) {   // after the last P V: O is final once these MMAs complete
@@ -542,7 +546,7 @@ __device__ void mma_pv_role(const Ctx& c) {
 #pragma unroll
         for (int k = 0; k < kChunk / 16; ++k)   // P of cells 16k..16k+15: columns 8(k&1) + 32(k>>1)
             tc::mma_ts_elect(tO, tP + 8 * (k & 1) + 32 * (k >> 1), dv + ((k * 2048) >> 4), idO,
-                             (t > 0 || k > 0) ? 1u : 0u);
+                             (t > 1 || k > 0) ? 1u : 0u);
         tc::commit_elect(bar(c, BAR_V_EMPTY + b));
         tc::commit_elect(bar(c, BAR_PV_DONE + sb));
     }
@@ -620,11 +624,6 @@ __device__ __forceinline__ void exp16(const uint32_t* s, const float* vs, float2
     }
 }
 
-// Brings a row sum kept relative to max `from` to max `to` (both finite, or the
-// sum is 0).
-__device__ __forceinline__ float rebase(float l, float from, float to) {
-    return (l == 0.f || from == to) ? l : l * fast_exp2(from - to);
-}
 
 // Softmax warp of set `set` (chunks t % 2 == set), half `hf` (0: columns [0,32)
 // of each chunk, 1: [32,64)) over lane quadrant `quad` (rows 32*quad + lane).
@@ -636,7 +635,7 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const size_t row_off = ((size_t)(c.q_begin + j) * c.n_heads + (size_t)c.h * kHeadsPerKv + hq) * kHeadDim;
     float* xchg = smem_f(c, kOffXchg);     // [set][parity][half][row]
-    float* mslot = smem_f(c, kOffMslot);   // [chunk parity][row]
+    float* mslot = smem_f(c, kOffMslot);   // [set][row]: each set's final running max
     float* lsum = smem_f(c, kOffLsum);     // [set * 2 + half][row]
     float* rsv = smem_f(c, kOffRs);        // [row]
     // Set 0 writes Q row r, this warp's 64-element half, as FP16 pairs into TMEM
@@ -691,10 +690,11 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
     const bool qscaled = __any_sync(0xffffffffu, rs != 1.f);
     // Weights are kept in log2 units, x = q.k * ks + ev, and masked after all
     // scaling, so p = 2^(x - m) holds for any sm_scale (0 gives equal weights; no
-    // -inf is ever multiplied).  m is the running max handed between the sets;
-    // this warp's sum l is relative to ml, the m it last used.
+    // -inf is ever multiplied).  Each set keeps its own running max m, its own
+    // O and, per warp, the sum l of its half's weights relative to m; the two
+    // sets are combined at the end.
     const float thresh = kRescaleLog2;
-    float ml = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = set;; t += 2) {
         const bool aborted = *c.abort_flag != 0;   // read after the previous pair barrier
@@ -704,9 +704,9 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
         const RawTab* T = raw_tab(c, ts);
         if (T->end) {   // past the last chunk; the set at the chunk count tells the P V issuer
             // That arrival waits, like a chunk's own, for the buffer's previous P V
-            // (chunk t-4) to complete: the set's warps do not run in step, and an
-            // mbarrier only counts arrivals, so it must not be counted with a slower
-            // warp's arrival for chunk t-4.
+            // (chunk t-3) to complete: the warps do not run in step, and an mbarrier
+            // only counts arrivals, so it must not be counted with a slower warp's
+            // arrival for chunk t-3.
             const bool signal = t == *c.n_final;
             if (signal && t >= kNSb &&
                 !(ok = wait_addr(c, bar(c, BAR_PV_DONE + sb), ((t - kNSb) / kNSb) & 1)))
@@ -743,18 +743,9 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
         xb[hf * kRows + r] = fmaxf(mx, my);
         if (!(ok = pair_sync(set, quad, aborted))) break;
         const float m_chunk = fmaxf(fmaxf(mx, my), xb[(hf ^ 1) * kRows + r]);
-        // the running max after chunk t-1, from the other set
-        float m = -INFINITY;
-        if (t > 0) {
-            if (!(ok = wait_addr(c, bar(c, BAR_M_READY + ((t - 1) & 1)), ((t - 1) >> 1) & 1))) break;
-            m = mslot[((t - 1) & 1) * kRows + r];
-        }
         const float m_new = fmaxf(m, m_chunk);
         const bool need = (m != -INFINITY) && (m_new > m + thresh);
         const float m_use = (m == -INFINITY || need) ? m_new : m;
-        if (hf == 0) mslot[(t & 1) * kRows + r] = m_use;
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(c, BAR_M_READY + (t & 1)));
         const float alpha = need ? fast_exp2(m - m_new) : 1.f;
         const float m_sub = m_use == -INFINITY ? 0.f : m_use;
         uint32_t p[16];
@@ -773,20 +764,18 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
 #pragma unroll
             for (int v = 0; v < 8; ++v) p[8 + v] = 0u;
         }
-        if (m_use != -INFINITY) {
-            l = rebase(l, ml, m_use) + ((la.x + la.y) + (lb.x + lb.y)) * vinv;
-            ml = m_use;
-        }
+        l = l * alpha + ((la.x + la.y) + (lb.x + lb.y)) * vinv;
+        m = m_use;
         tc::tmem_st16(tS + 32 * hf, p);
         if (__any_sync(0xffffffffu, need)) {
-            // O must hold every earlier P V before it is rescaled: wait for PV(t-1);
-            // this warp rescales its half of O's columns
-            if (!(ok = wait_addr(c, bar(c, BAR_PV_DONE + (t - 1) % kNSb), ((t - 1) / kNSb) & 1))) break;
+            // this set's O must hold every earlier P V of the set before it is
+            // rescaled: wait for P(t-2) V; this warp rescales its half of the set's O
+            if (!(ok = wait_addr(c, bar(c, BAR_PV_DONE + (t - 2) % kNSb), ((t - 2) / kNSb) & 1))) break;
             tc::fence_after_sync();
 #pragma unroll 1
             for (int q8 = 0; q8 < 4; ++q8) {
                 uint32_t o[16];
-                const uint32_t ta = c.tmem + lane_base + kColO + 64 * hf + 16 * q8;
+                const uint32_t ta = c.tmem + lane_base + kColO + 128 * set + 64 * hf + 16 * q8;
                 tc::tmem_ld16(ta, o);
                 tc::tmem_wait_ld();
 #pragma unroll
@@ -815,33 +804,40 @@ __device__ void softmax_role(const Ctx& c, int set, int hf, int quad, int lane) 
             for (int v = 0; v < 8; ++v) reinterpret_cast<float4*>(out)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
-    // the final running max (chunk n-1's), from whichever set took that chunk
-    const int tl = n - 1;
-    if (!wait_addr(c, bar(c, BAR_M_READY + (tl & 1)), (tl >> 1) & 1)) {
-        leave_all(set, quad);
-        return;
-    }
-    const float mf = mslot[(tl & 1) * kRows + r];
-    // total weight of the row: the four warps' sums, brought to the final max
-    lsum[(2 * set + hf) * kRows + r] = ml == -INFINITY ? 0.f : rebase(l, ml, mf);
+    // Combine the two sets: M = max(m_0, m_1); each set weighs 2^(m_s - M) (0 for a
+    // set with no weight on this row, whose O is not read); the row's total weight is
+    // the four warps' sums so weighted.
+    if (hf == 0) mslot[set * kRows + r] = m;
+    lsum[(2 * set + hf) * kRows + r] = l;
     if (*c.abort_flag != 0) {
         leave_all(set, quad);
         return;
     }
     named_sync<128>(7 + quad);
-    const float l_tot = (lsum[r] + lsum[kRows + r]) + (lsum[2 * kRows + r] + lsum[3 * kRows + r]);
+    const float m0 = mslot[r], m1 = mslot[kRows + r];
+    const float mm = fmaxf(m0, m1);
+    const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - mm), w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - mm);
+    const float l_tot = w0 * (lsum[r] + lsum[kRows + r]) + w1 * (lsum[2 * kRows + r] + lsum[3 * kRows + r]);
     if (!wait_addr(c, bar(c, BAR_O_DONE), 0)) return;
     tc::fence_after_sync();
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-    uint32_t o[32];
-    tc::tmem_ld32(c.tmem + lane_base + kColO + ocol, o);
+    const float s0 = w0 * inv, s1 = w1 * inv;
+    uint32_t o0[32], o1[32];
+    tc::tmem_ld32(c.tmem + lane_base + kColO + ocol, o0);
+    tc::tmem_ld32(c.tmem + lane_base + kColO + 128 + ocol, o1);
     tc::tmem_wait_ld();
     if (row_ok) {
 #pragma unroll
+        for (int v = 0; v < 32; ++v) {
+            const float a0 = s0 != 0.f ? __uint_as_float(o0[v]) * s0 : 0.f;
+            const float a1 = s1 != 0.f ? __uint_as_float(o1[v]) * s1 : 0.f;
+            o0[v] = __float_as_uint(a0 + a1);
+        }
+#pragma unroll
         for (int v = 0; v < 8; ++v)
             reinterpret_cast<float4*>(out)[v] =
-                make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                            __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+                make_float4(__uint_as_float(o0[4 * v]), __uint_as_float(o0[4 * v + 1]), __uint_as_float(o0[4 * v + 2]),
+                            __uint_as_float(o0[4 * v + 3]));
     }
 }
 
@@ -894,7 +890,6 @@ __global__ void __launch_bounds__(32 * kWarps, 1) attn_sm_kernel(const __grid_co
             tc::mbar_init(bar(c, BAR_P_READY + b), kSetWarps);
             tc::mbar_init(bar(c, BAR_PV_DONE + b), 1);
         }
-        for (int b = 0; b < 2; ++b) tc::mbar_init(bar(c, BAR_M_READY + b), kSetWarps);
         tc::mbar_init(bar(c, BAR_O_DONE), 1);
         tc::mbar_init(bar(c, BAR_Q_READY), kSetWarps);   // set 0's softmax warps
         tc::mbar_init(bar(c, BAR_DRAIN_S), 1);
