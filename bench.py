@@ -134,15 +134,16 @@ def algorithmic(w, union_count):
                 mean_union=float(U.mean()), union_ratio=float(U.mean() / w.sel_count.mean()))
 
 
-def read_traffic(profile: str, kernel: str, sources):
+def read_traffic(profile: str, kernel: str, sources, pdir: str = None):
     """DRAM bytes per launch from the committed ncu summary profiles/<profile>.txt
-    (one kernel on one workload), if it names `kernel` and the kernel's sources
-    still hash to what the capture recorded; else None.  Returns (bytes, hash)."""
+    (one kernel on one workload; `pdir` replaces profiles/), if it names `kernel`
+    and the kernel's sources still hash to what the capture recorded; else None.
+    Returns (bytes, hash)."""
     h = hashlib.sha256()
     for s in sources:
         h.update(open(os.path.join(ROOT, s), "rb").read())
     digest = h.hexdigest()[:16]
-    path = os.path.join(ROOT, "profiles", profile + ".txt")
+    path = os.path.join(pdir or os.path.join(ROOT, "profiles"), profile + ".txt")
     if not os.path.isfile(path):
         return None, digest
     txt = open(path).read()
