@@ -159,3 +159,22 @@ def test_select_scale_signs_and_ranges(qsa):
     assert st == 0
     ref = oracle.attn_ref(w.q, w.k_pool, w.v_pool, ks, vs, w.page_table, w.sel, w.sel_count, w.n_kv, 0.05)
     check_close(got, ref, "scale signs and ranges")
+
+
+def test_select_zero_scale_is_the_mean_of_v(qsa):
+    """sm_scale = 0 makes every selected, resident cell weigh the same: each row is the
+    plain mean of its cells' dequantised V (a closed form, computed here in numpy)."""
+    w = gen.make(2, n_q=24, nonresident_frac=0.1, seed=41)
+    got, st = run_sel(qsa, w, sm_scale=0.0)
+    assert st == 0
+    v = w.v_pool.astype(np.float64) * w.v_scale.astype(np.float64)[..., None]   # [page][kv][cell][d]
+    ref = np.zeros_like(got, dtype=np.float64)
+    for i in range(w.n_q):
+        cells = w.sel[i, :w.sel_count[i]]
+        pages = w.page_table[cells >> 6]
+        keep = pages >= 0
+        for kh in range(w.n_kv):
+            rows = v[pages[keep], kh, cells[keep] & 63]
+            if len(rows):
+                ref[i, kh * 12:(kh + 1) * 12] = rows.mean(axis=0)
+    check_close(got, ref, "sm_scale = 0")
