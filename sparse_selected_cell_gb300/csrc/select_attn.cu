@@ -32,10 +32,11 @@
 //     scaling, as in the union kernel): each lane's K operand is one 32-bit word
 //     of the INT8 row (the head dimension is permuted inside every 16-wide k
 //     step, for Q and K alike), converted exactly in registers (|int8| <= 128
-//     fits FP16); the K scale (times sm_scale and log2 e)
-//     multiplies each score column in FP32, unselected / masked cells are -inf,
-//     the online softmax runs in the exp2 domain with the same lazy rescale as
-//     the union kernel, and P = p * (V scale) enters O += P V as BF16; V also
+//     fits FP16); the K scale (times sm_scale and log2 e) multiplies each score
+//     column in FP32, unselected / masked cells are -inf, the online softmax
+//     runs in the exp2 domain with the same lazy rescale as the union kernel
+//     (the row-max shuffles and the rescale behind one warp vote), and
+//     P = p * (V scale) enters O += P V as BF16; V also
 //     goes from the INT8 stage straight into the B fragments (ldmatrix.trans of
 //     byte pairs, the output columns permuted so that a lane's accumulators
 //     cover four consecutive dims), so the kernel writes no operand tile.
